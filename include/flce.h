@@ -1,0 +1,161 @@
+/*
+ * flce.h — fused linear cross-entropy on one GB300 GPU (sm_103a), C ABI.
+ *
+ * The operation (ms-swift PR #9784 "feat(sft): Add optional fused linear ce for
+ * qwen2/qwen3 on npu", sections Background, What this PR does and Mathematical
+ * Equivalence):
+ *
+ *     Z = X W^T                     X: N x H token hidden states, W: V x H
+ *     loss = reduce_i CE(Z_i, t_i)  per-row cross-entropy against target t_i
+ *     dX = dZ W,  dW = dZ^T X       dZ = (softmax(Z) - onehot(t)) * g / n_valid
+ *
+ * computed without ever holding the N x V logits.  The call surface mirrors
+ * `linear_cross_entropy(hidden, weight, labels, ignore_index=-100, shift=True,
+ * reduction="mean")` with W stored (vocab, hidden) (Qwen3.5-35B-A3B LoRA SFT
+ * blog post, listing `_patch_model_with_cce`), and gradients are accumulated in
+ * FP32 and rounded to bf16 only at the end (Megatron-LM PR #2739 "[Dev] Fix
+ * Linear-Cross-Entropy Convergence Issue", section 2).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" are CUDA device pointers on the current device;
+ *     the caller allocates and owns every buffer.  The library allocates no
+ *     device memory and keeps no state between calls.
+ *   - Everything is enqueued on `stream` and runs asynchronously; no entry point
+ *     synchronises except flce_get_error.
+ *   - X and W are bf16, row-major, rows contiguous: X[i*H + h], W[v*H + h].
+ *     H must be a multiple of 8 (16-byte rows for the tensor-memory copies) and
+ *     both base pointers 16-byte aligned.
+ *   - labels are int64.  With shift != 0, row s of each length-seq_len sequence
+ *     is scored against labels[s+1] of the same sequence and the last row of
+ *     every sequence is ignored; N must be a multiple of seq_len (seq_len <= 0
+ *     means one sequence of N rows).  With shift == 0, row i uses labels[i].
+ *   - A target equal to ignore_index is ignored, even if it lies in [0, V).  A
+ *     target outside [0, V) that is not ignore_index sets
+ *     FLCE_ERR_LABEL_OUT_OF_RANGE in the workspace error word (see
+ *     flce_get_error) and its row is treated as ignored; the call still
+ *     completes.
+ *   - reduction MEAN divides by n_valid, the number of valid targets in the
+ *     whole call; with n_valid == 0 the loss and gradients are 0.
+ *   - Host-detectable errors (null pointers, bad sizes, short workspace, a
+ *     device older than sm_103) are returned at once and nothing is enqueued.
+ *     No exception crosses the ABI and no kernel traps.
+ */
+#ifndef FLCE_H
+#define FLCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st* flce_stream_t;
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, N % seq_len != 0 ... */
+  FLCE_ERR_UNSUPPORTED_SHAPE = 2,  /* H % 8 != 0, H/V/N outside the supported range */
+  FLCE_ERR_WORKSPACE_TOO_SMALL = 3,
+  FLCE_ERR_LABEL_OUT_OF_RANGE = 4, /* device-detected: reported by flce_get_error */
+  FLCE_ERR_TIMEOUT = 5,            /* device-detected: a bounded wait ran out */
+  FLCE_ERR_CUDA = 6,               /* a CUDA runtime call failed */
+  FLCE_ERR_UNSUPPORTED_DEVICE = 7  /* not an sm_103 (GB300-class) device */
+} flce_status;
+
+typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 } flce_reduction;
+
+/*
+ * Bytes of device workspace flce_forward and flce_backward need for these
+ * sizes (one buffer serves both; it need not survive from forward to
+ * backward).  It is O(N*H + Vb*H + N*V/1024 + tiles), never O(N*V): FP32
+ * accumulators for dX and for one vocab band of dW, a bounded bf16 block of
+ * dZ, and per-row partial log-sum-exps.  Returns 0 for invalid sizes.
+ */
+size_t flce_workspace_size(int64_t N, int64_t H, int64_t V);
+
+/*
+ * Forward: loss, per-row log-sum-exp and the valid-target count.
+ *
+ *   X, W            device, bf16, see conventions.
+ *   labels          device, int64 [N].
+ *   loss            device float, 1 element: mean or sum of the per-row
+ *                   losses lse_i - z_{i,t_i} over valid rows (deterministic).
+ *   lse             device float [N]: log sum_j exp(Z_ij) for every row, valid
+ *                   or not (it does not depend on labels).
+ *   n_valid         device int64, 1 element (exact).
+ *   workspace       device, >= flce_workspace_size(N, H, V) bytes, 256-byte
+ *                   aligned; its error word is reset at the start of the call.
+ * N == 0 is allowed: loss = 0 and n_valid = 0.
+ */
+flce_status flce_forward(const void* X, const void* W, const int64_t* labels,
+                         int64_t N, int64_t H, int64_t V, int64_t seq_len,
+                         int64_t ignore_index, int shift, flce_reduction reduction,
+                         float* loss, float* lse, int64_t* n_valid,
+                         void* workspace, size_t workspace_bytes, flce_stream_t stream);
+
+/*
+ * Backward: dX and/or dW for upstream gradient g of the loss.
+ *
+ *   lse, n_valid    device, as written by flce_forward for the same inputs.
+ *   grad_loss       device float, 1 element: g = d(outer loss)/d(loss).
+ *   dX              device bf16 [N, H] or NULL to skip it (e.g. when only W is
+ *                   trained); written, not accumulated.
+ *   dW              device bf16 [V, H] or NULL to skip it (a frozen LM head,
+ *                   as in LoRA fine-tuning); written, not accumulated.
+ * Gradients are accumulated in FP32 and rounded to bf16 (round to nearest even)
+ * once, after the scale g / n_valid (mean) or g (sum) is applied in FP32.
+ * The other arguments have the same meaning as in flce_forward.
+ */
+flce_status flce_backward(const void* X, const void* W, const int64_t* labels,
+                          int64_t N, int64_t H, int64_t V, int64_t seq_len,
+                          int64_t ignore_index, int shift, flce_reduction reduction,
+                          const float* lse, const int64_t* n_valid, const float* grad_loss,
+                          void* dX, void* dW,
+                          void* workspace, size_t workspace_bytes, flce_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and returns the device error word written
+ * by the last flce_forward / flce_backward call that used this workspace:
+ * FLCE_OK, FLCE_ERR_LABEL_OUT_OF_RANGE or FLCE_ERR_TIMEOUT (the first one
+ * raised wins; a timeout outranks a label error).  FLCE_ERR_CUDA if the
+ * synchronisation itself fails.
+ */
+flce_status flce_get_error(const void* workspace, flce_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* flce_status_string(flce_status status);
+
+/*
+ * Limit, in nanoseconds, on every wait inside the library's kernels (default
+ * 2e9).  A wait that runs out records FLCE_ERR_TIMEOUT and its kernel returns
+ * early.  Values <= 0 restore the default.  Process-wide; not thread-safe
+ * against concurrent calls.
+ */
+void flce_set_wait_limit_ns(int64_t limit_ns);
+
+/*
+ * Tuning: caps the backward's dZ block at `max_rows` token rows (rounded down
+ * to a multiple of 128, at least 128) and `max_block_elems` bf16 elements
+ * (default 8192 rows and 16 Mi elements, a 32 MB block that stays in L2).
+ * Smaller blocks mean less workspace and more FP32 accumulation traffic.
+ * Values <= 0 restore the defaults.  Process-wide; flce_workspace_size and the
+ * calls that use the workspace must see the same setting.
+ */
+void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems);
+
+/*
+ * Self-test of the bounded-wait path: enqueues one small kernel that waits on
+ * a barrier nothing will ever complete, with a limit of `limit_ns`, then
+ * records FLCE_ERR_TIMEOUT in the workspace error word and returns cleanly.
+ * flce_get_error(workspace, stream) then reports FLCE_ERR_TIMEOUT.  Needs
+ * workspace_bytes >= 256.
+ */
+flce_status flce_selftest_wait_timeout(int64_t limit_ns, void* workspace,
+                                       size_t workspace_bytes, flce_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLCE_H */

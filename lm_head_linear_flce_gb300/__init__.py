@@ -1,0 +1,224 @@
+"""Fused linear cross-entropy for one GB300 GPU.
+
+A thin Python binding over the C ABI in ``include/flce.h`` (``libflce.so``).
+It only marshals arguments: tensors become device pointers, the stream is
+torch's current stream, and the workspace comes from torch's caching
+allocator.  Every step of the computation runs in the library's kernels; there
+is no fallback path.  If the library has not been built, every call raises.
+
+The user-facing call mirrors ``linear_cross_entropy(hidden, weight, labels,
+ignore_index=-100, shift=True, reduction="mean")`` from the Qwen3.5-35B-A3B
+LoRA SFT blog post (listing `_patch_model_with_cce`), with W stored
+(vocab, hidden).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "FlceError", "library", "library_path", "workspace_size", "flce_forward", "flce_backward",
+    "flce_get_error", "flce_selftest_wait_timeout", "flce_set_wait_limit_ns",
+    "flce_set_backward_block",
+    "linear_cross_entropy", "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "_lib", "libflce.so")
+
+STATUS = {
+    0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED_SHAPE",
+    3: "FLCE_ERR_WORKSPACE_TOO_SMALL", 4: "FLCE_ERR_LABEL_OUT_OF_RANGE", 5: "FLCE_ERR_TIMEOUT",
+    6: "FLCE_ERR_CUDA", 7: "FLCE_ERR_UNSUPPORTED_DEVICE",
+}
+_REDUCTION = {"mean": 0, "sum": 1}
+
+
+class FlceError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded libflce.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise RuntimeError(
+            f"{library_path} is missing: build it with lm_head_linear_flce_gb300._build.build() "
+            "(nvcc, sm_103a); there is no fallback implementation")
+    lib = ctypes.CDLL(library_path)
+    c_i64, c_sz, c_p, c_int, c_f = (ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p,
+                                    ctypes.c_int, ctypes.c_float)
+    lib.flce_workspace_size.argtypes = [c_i64, c_i64, c_i64]
+    lib.flce_workspace_size.restype = c_sz
+    lib.flce_forward.argtypes = [c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i64, c_i64, c_int, c_int,
+                                 c_p, c_p, c_p, c_p, c_sz, c_p]
+    lib.flce_forward.restype = c_int
+    lib.flce_backward.argtypes = [c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i64, c_i64, c_int, c_int,
+                                  c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]
+    lib.flce_backward.restype = c_int
+    lib.flce_get_error.argtypes = [c_p, c_p]
+    lib.flce_get_error.restype = c_int
+    lib.flce_status_string.argtypes = [c_int]
+    lib.flce_status_string.restype = ctypes.c_char_p
+    lib.flce_set_wait_limit_ns.argtypes = [c_i64]
+    lib.flce_set_wait_limit_ns.restype = None
+    lib.flce_set_backward_block.argtypes = [c_i64, c_i64]
+    lib.flce_set_backward_block.restype = None
+    lib.flce_selftest_wait_timeout.argtypes = [c_i64, c_p, c_sz, c_p]
+    lib.flce_selftest_wait_timeout.restype = c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise FlceError(status, where)
+
+
+def workspace_size(N: int, H: int, V: int) -> int:
+    return int(library().flce_workspace_size(N, H, V))
+
+
+def _workspace(N, H, V, device, workspace):
+    need = workspace_size(N, H, V)
+    if need == 0:
+        raise FlceError(2, "flce_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace
+
+
+def _check_inputs(X, W, labels):
+    for name, t, dt in (("hidden", X, torch.bfloat16), ("weight", W, torch.bfloat16),
+                        ("labels", labels, torch.int64)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != dt:
+            raise ValueError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if X.dim() != 2 or W.dim() != 2 or labels.dim() != 1:
+        raise ValueError("expected X [N,H], W [V,H], labels [N]")
+    if X.shape[1] != W.shape[1] or labels.shape[0] != X.shape[0]:
+        raise ValueError("shape mismatch between X, W and labels")
+
+
+def flce_forward(X, W, labels, *, seq_len=None, ignore_index=-100, shift=False,
+                 reduction="mean", workspace=None):
+    """Calls flce_forward; returns (loss [1] f32, lse [N] f32, n_valid [1] i64, workspace)."""
+    _check_inputs(X, W, labels)
+    N, H = X.shape
+    V = W.shape[0]
+    dev = X.device
+    ws = _workspace(N, H, V, dev, workspace)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    st = library().flce_forward(_ptr(X), _ptr(W), _ptr(labels), N, H, V, int(seq_len or 0),
+                                int(ignore_index), int(bool(shift)), _REDUCTION[reduction],
+                                _ptr(loss), _ptr(lse), _ptr(n_valid), _ptr(ws), ws.numel(),
+                                _stream(dev))
+    _check(st, "flce_forward")
+    return loss, lse, n_valid, ws
+
+
+def flce_backward(X, W, labels, lse, n_valid, grad_loss, *, seq_len=None, ignore_index=-100,
+                  shift=False, reduction="mean", need_dX=True, need_dW=True, workspace=None,
+                  dX=None, dW=None):
+    """Calls flce_backward; returns (dX or None, dW or None, workspace)."""
+    _check_inputs(X, W, labels)
+    N, H = X.shape
+    V = W.shape[0]
+    dev = X.device
+    ws = _workspace(N, H, V, dev, workspace)
+    if need_dX and dX is None:
+        dX = torch.empty_like(X)
+    if need_dW and dW is None:
+        dW = torch.empty_like(W)
+    g = grad_loss.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+    st = library().flce_backward(_ptr(X), _ptr(W), _ptr(labels), N, H, V, int(seq_len or 0),
+                                 int(ignore_index), int(bool(shift)), _REDUCTION[reduction],
+                                 _ptr(lse), _ptr(n_valid), _ptr(g),
+                                 _ptr(dX if need_dX else None), _ptr(dW if need_dW else None),
+                                 _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "flce_backward")
+    return (dX if need_dX else None), (dW if need_dW else None), ws
+
+
+def flce_get_error(workspace) -> int:
+    """Synchronises the current stream and returns the workspace's error status."""
+    return int(library().flce_get_error(_ptr(workspace), _stream(workspace.device)))
+
+
+def flce_set_wait_limit_ns(limit_ns: int) -> None:
+    library().flce_set_wait_limit_ns(int(limit_ns))
+
+
+def flce_set_backward_block(max_rows: int = 0, max_block_elems: int = 0) -> None:
+    """Caps the backward's dZ block (0 restores the defaults); see include/flce.h."""
+    library().flce_set_backward_block(int(max_rows), int(max_block_elems))
+
+
+def flce_selftest_wait_timeout(limit_ns: int, workspace) -> int:
+    return int(library().flce_selftest_wait_timeout(int(limit_ns), _ptr(workspace),
+                                                    workspace.numel(),
+                                                    _stream(workspace.device)))
+
+
+class _FusedLinearCE(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, X, W, labels, seq_len, ignore_index, shift, reduction):
+        loss, lse, n_valid, _ = flce_forward(X, W, labels, seq_len=seq_len,
+                                             ignore_index=ignore_index, shift=shift,
+                                             reduction=reduction)
+        ctx.save_for_backward(X, W, labels, lse, n_valid)
+        ctx.cfg = (seq_len, ignore_index, shift, reduction)
+        return loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad):
+        X, W, labels, lse, n_valid = ctx.saved_tensors
+        seq_len, ignore_index, shift, reduction = ctx.cfg
+        dX, dW, _ = flce_backward(X, W, labels, lse, n_valid, grad.detach(), seq_len=seq_len,
+                                  ignore_index=ignore_index, shift=shift, reduction=reduction,
+                                  need_dX=ctx.needs_input_grad[0],
+                                  need_dW=ctx.needs_input_grad[1])
+        return dX, dW, None, None, None, None, None
+
+
+def linear_cross_entropy(hidden, weight, labels, ignore_index=-100, shift=False,
+                         reduction="mean", seq_len=None):
+    """Cross-entropy of hidden @ weight.T against labels, without the logits.
+
+    hidden: bf16 [B, S, H] or [N, H]; weight: bf16 [V, H]; labels: int64 [B, S]
+    or [N].  With shift=True, position s of each sequence is scored against
+    labels[s+1] and the last position is ignored (for 3-D hidden the sequence
+    length is S; for 2-D, seq_len or one sequence).  Returns a 0-dim float32
+    loss that back-propagates to hidden and weight.
+    """
+    if reduction not in _REDUCTION:
+        raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
+    if hidden.dim() == 3:
+        B, S, H = hidden.shape
+        seq_len = S
+        hidden = hidden.reshape(B * S, H)
+        labels = labels.reshape(B * S)
+    return _FusedLinearCE.apply(hidden.contiguous(), weight.contiguous(), labels.contiguous(),
+                                seq_len, ignore_index, shift, reduction)

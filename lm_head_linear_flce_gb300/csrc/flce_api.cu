@@ -1,0 +1,416 @@
+// C ABI of the fused linear cross-entropy library: argument checks, the
+// problem plan and workspace layout, tensor-map encoding and the launch
+// sequences of flce_forward / flce_backward.  See include/flce.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+
+#include "../../include/flce.h"
+#include "flce_internal.h"
+
+namespace flce {
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;
+constexpr int64_t kMaxH = 1 << 16;
+constexpr int64_t kDefaultDzBlockElems = int64_t{16} << 20;  // bf16 dZ block: 32 MB, L2-resident
+constexpr int64_t kDefaultMaxBlockRows = 8192;
+constexpr size_t kAlign = 256;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
+std::atomic<int64_t> g_block_rows{kDefaultMaxBlockRows};
+std::atomic<int64_t> g_block_elems{kDefaultDzBlockElems};
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer][inner] matrix with 128-byte
+// swizzle; out-of-bounds elements read as zero.
+bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+flce_status device_info(DeviceInfo* d) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  if (dev >= 0 && dev < 64 && have[dev]) {
+    *d = cache[dev];
+    return d->ok ? FLCE_OK : FLCE_ERR_UNSUPPORTED_DEVICE;
+  }
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  d->sms = sms;
+  d->ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) {
+    cache[dev] = *d;
+    have[dev] = true;
+  }
+  return d->ok ? FLCE_OK : FLCE_ERR_UNSUPPORTED_DEVICE;
+}
+
+flce_status check_common(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t seq_len, int shift,
+                         flce_reduction reduction, void* ws, size_t ws_bytes, Plan* plan) {
+  if (N < 0 || H <= 0 || V <= 0) return FLCE_ERR_INVALID_ARG;
+  if (reduction != FLCE_REDUCTION_MEAN && reduction != FLCE_REDUCTION_SUM)
+    return FLCE_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > kMaxH || N > kMaxDim || V > kMaxDim) return FLCE_ERR_UNSUPPORTED_SHAPE;
+  if (!ws) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!X || !W || !labels)) return FLCE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15)
+    return FLCE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) return FLCE_ERR_INVALID_ARG;
+  if (shift && N > 0) {
+    const int64_t S = seq_len > 0 ? seq_len : N;
+    if (N % S != 0) return FLCE_ERR_INVALID_ARG;
+  }
+  if (!make_plan(N, H, V, plan)) return FLCE_ERR_UNSUPPORTED_SHAPE;
+  if (ws_bytes < plan->total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  return FLCE_OK;
+}
+
+#define FLCE_CUDA(x)                         \
+  do {                                       \
+    if ((x) != cudaSuccess) return FLCE_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
+  if (N < 0 || H <= 0 || V <= 0) return false;
+  std::memset(p, 0, sizeof(*p));
+  p->N = N;
+  p->H = H;
+  p->V = V;
+  p->m_tiles = static_cast<int>(cdiv(N, kBM));
+  p->v_tiles = static_cast<int>(cdiv(V, kBN));
+  p->v_units = static_cast<int>(cdiv(p->v_tiles, kFwdGroup));
+  p->h_tiles = static_cast<int>(cdiv(H, kBN));
+  // Backward blocking: a token block of Nb rows x a vocab block of Vb columns
+  // of dZ is formed at a time (bf16, at most kDzBlockElems).  All rows in one
+  // block when they fit, so dW needs no FP32 accumulator across blocks.
+  const int64_t max_rows = g_block_rows.load();
+  const int64_t max_elems = g_block_elems.load();
+  const int64_t n_pad = std::max<int64_t>(int64_t{p->m_tiles} * kBM, kBM);
+  if (n_pad <= max_rows) {
+    p->Nb = n_pad;
+  } else {
+    const int64_t nblk = cdiv(n_pad, max_rows);
+    p->Nb = cdiv(std::max(p->m_tiles, 1), nblk) * kBM;
+  }
+  const int64_t v_pad = int64_t{p->v_tiles} * kBN;
+  p->Vb = std::min<int64_t>(v_pad, std::max<int64_t>(kBN, max_elems / p->Nb / kBN * kBN));
+  p->n_blocks = N > 0 ? static_cast<int>(cdiv(N, p->Nb)) : 0;
+  p->v_blocks = static_cast<int>(cdiv(V, p->Vb));
+  p->multi_n = p->n_blocks > 1;
+
+  size_t off = 0;
+  p->off_err = off;
+  off = align_up(off + 16);
+  p->off_t = off;
+  off = align_up(off + static_cast<size_t>(N) * 4);
+  const size_t shared_start = off;
+  // forward view
+  p->off_zt = off;
+  off = align_up(off + static_cast<size_t>(N) * 4);
+  p->off_part = off;
+  off = align_up(off + static_cast<size_t>(p->v_units) * N * 8);
+  p->off_lossp = off;
+  off = align_up(off + static_cast<size_t>(cdiv(N, 256) + 1) * 8);
+  const size_t fwd_end = off;
+  // backward view (overlaps the forward view: the workspace need not persist)
+  off = shared_start;
+  p->off_dxf = off;
+  if (p->v_blocks > 1) off = align_up(off + static_cast<size_t>(N) * H * 4);
+  p->off_dwf = off;
+  if (p->multi_n) off = align_up(off + static_cast<size_t>(p->Vb) * H * 4);
+  p->off_dz = off;
+  off = align_up(off + static_cast<size_t>(p->Nb) * p->Vb * 2);
+  p->total = std::max(fwd_end, off);
+  return true;
+}
+
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+const char* flce_status_string(flce_status s) {
+  switch (s) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARG: return "FLCE_ERR_INVALID_ARG";
+    case FLCE_ERR_UNSUPPORTED_SHAPE: return "FLCE_ERR_UNSUPPORTED_SHAPE";
+    case FLCE_ERR_WORKSPACE_TOO_SMALL: return "FLCE_ERR_WORKSPACE_TOO_SMALL";
+    case FLCE_ERR_LABEL_OUT_OF_RANGE: return "FLCE_ERR_LABEL_OUT_OF_RANGE";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA";
+    case FLCE_ERR_UNSUPPORTED_DEVICE: return "FLCE_ERR_UNSUPPORTED_DEVICE";
+  }
+  return "FLCE_ERR_UNKNOWN";
+}
+
+size_t flce_workspace_size(int64_t N, int64_t H, int64_t V) {
+  if (N < 0 || H <= 0 || V <= 0 || H % 8 != 0 || H > kMaxH || N > kMaxDim || V > kMaxDim)
+    return 0;
+  Plan p;
+  if (!make_plan(N, H, V, &p)) return 0;
+  return p.total;
+}
+
+void flce_set_wait_limit_ns(int64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns > 0 ? static_cast<unsigned long long>(limit_ns)
+                                     : kDefaultWaitNs);
+}
+
+void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems) {
+  g_block_rows.store(max_rows > 0 ? std::max<int64_t>(max_rows / kBM * kBM, kBM)
+                                  : kDefaultMaxBlockRows);
+  g_block_elems.store(max_block_elems > 0 ? max_block_elems : kDefaultDzBlockElems);
+}
+
+flce_status flce_forward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t seq_len, int64_t ignore_index, int shift,
+                         flce_reduction reduction, float* loss, float* lse, int64_t* n_valid,
+                         void* workspace, size_t workspace_bytes, flce_stream_t stream) {
+  Plan p;
+  flce_status st = check_common(X, W, labels, N, H, V, seq_len, shift, reduction, workspace,
+                                workspace_bytes, &p);
+  if (st != FLCE_OK) return st;
+  if (!loss || !n_valid || (N > 0 && !lse)) return FLCE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* err = reinterpret_cast<int*>(ws + p.off_err);
+  FLCE_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  FLCE_CUDA(cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s));
+  if (N == 0) {
+    FLCE_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    return FLCE_OK;
+  }
+  int* targets = reinterpret_cast<int*>(ws + p.off_t);
+  float* zt = reinterpret_cast<float*>(ws + p.off_zt);
+  float2* part = reinterpret_cast<float2*>(ws + p.off_part);
+  double* lossp = reinterpret_cast<double*>(ws + p.off_lossp);
+  const int S = static_cast<int>(seq_len > 0 ? seq_len : N);
+  FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index,
+                                static_cast<int>(V), targets,
+                                reinterpret_cast<long long*>(n_valid), err, s));
+
+  CUtensorMap tx, tw;
+  if (!make_tmap(&tx, X, H, N, H * 2, kBK, kBM) || !make_tmap(&tw, W, H, V, H * 2, kBK, kBN))
+    return FLCE_ERR_CUDA;
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.tiles_m = p.m_tiles;
+  a.tiles_n = p.v_tiles;
+  a.group = kFwdGroup;
+  a.units = p.m_tiles * p.v_units;
+  a.k_blocks = static_cast<int>(cdiv(H, kBK));
+  a.N = static_cast<int>(N);
+  a.H = static_cast<int>(H);
+  a.V = static_cast<int>(V);
+  a.targets = targets;
+  a.partials = part;
+  a.zt = zt;
+  a.err = err;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  FLCE_CUDA(launch_gemm(kKindFwd, tx, tw, a, std::min(a.units, dev.sms), s));
+  int nblocks = 0;
+  FLCE_CUDA(launch_merge_lse(part, p.v_units, static_cast<int>(N), zt, targets, lse, lossp, s,
+                             &nblocks));
+  FLCE_CUDA(launch_finalize_loss(lossp, nblocks, reinterpret_cast<const long long*>(n_valid),
+                                 reduction == FLCE_REDUCTION_SUM ? 1 : 0, loss, s));
+  return FLCE_OK;
+}
+
+flce_status flce_backward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                          int64_t H, int64_t V, int64_t seq_len, int64_t ignore_index, int shift,
+                          flce_reduction reduction, const float* lse, const int64_t* n_valid,
+                          const float* grad_loss, void* dX, void* dW, void* workspace,
+                          size_t workspace_bytes, flce_stream_t stream) {
+  Plan p;
+  flce_status st = check_common(X, W, labels, N, H, V, seq_len, shift, reduction, workspace,
+                                workspace_bytes, &p);
+  if (st != FLCE_OK) return st;
+  if (!n_valid || !grad_loss || (N > 0 && !lse)) return FLCE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dX) | reinterpret_cast<uintptr_t>(dW)) & 15)
+    return FLCE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != FLCE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* err = reinterpret_cast<int*>(ws + p.off_err);
+  FLCE_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  if (N == 0) {
+    if (dW) FLCE_CUDA(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 2, s));
+    return FLCE_OK;
+  }
+  if (!dX && !dW) return FLCE_OK;
+  const int red = reduction == FLCE_REDUCTION_SUM ? 1 : 0;
+  const long long* nv = reinterpret_cast<const long long*>(n_valid);
+  int* targets = reinterpret_cast<int*>(ws + p.off_t);
+  const int S = static_cast<int>(seq_len > 0 ? seq_len : N);
+  FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index,
+                                static_cast<int>(V), targets, nullptr, err, s));
+
+  float* dxf = reinterpret_cast<float*>(ws + p.off_dxf);
+  float* dwf = reinterpret_cast<float*>(ws + p.off_dwf);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + p.off_dz);
+  const bool dx_final = p.v_blocks == 1;
+  const bool dw_final = !p.multi_n;
+  if (dX && !dx_final) FLCE_CUDA(cudaMemsetAsync(dxf, 0, static_cast<size_t>(N) * H * 4, s));
+
+  CUtensorMap t_x_k, t_w_k, t_dz_k, t_w_mn, t_dz_mn, t_x_mn;
+  if (!make_tmap(&t_x_k, X, H, N, H * 2, kBK, kBM) ||
+      !make_tmap(&t_w_k, W, H, V, H * 2, kBK, kBN) ||
+      !make_tmap(&t_dz_k, dz, p.Vb, p.Nb, p.Vb * 2, kBK, kBM) ||
+      !make_tmap(&t_w_mn, W, H, V, H * 2, 64, 64) ||
+      !make_tmap(&t_dz_mn, dz, p.Vb, p.Nb, p.Vb * 2, 64, 64) ||
+      !make_tmap(&t_x_mn, X, H, N, H * 2, 64, 64))
+    return FLCE_ERR_CUDA;
+
+  GemmArgs base;
+  std::memset(&base, 0, sizeof(base));
+  base.N = static_cast<int>(N);
+  base.H = static_cast<int>(H);
+  base.V = static_cast<int>(V);
+  base.targets = targets;
+  base.lse = lse;
+  base.dz = dz;
+  base.dz_ld = static_cast<int>(p.Vb);
+  base.grad_loss = grad_loss;
+  base.n_valid = nv;
+  base.reduction = red;
+  base.err = err;
+  base.wait_limit_ns = g_wait_limit_ns.load();
+  base.group = 1;
+
+  for (int vb = 0; vb < p.v_blocks; ++vb) {
+    const int64_t col0 = int64_t{vb} * p.Vb;
+    const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
+    const int vt = static_cast<int>(cdiv(vext, kBN));
+    if (dW && !dw_final)
+      FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(vext) * H * 4, s));
+    for (int nb = 0; nb < p.n_blocks; ++nb) {
+      const int64_t row0 = int64_t{nb} * p.Nb;
+      const int64_t next = std::min<int64_t>(p.Nb, N - row0);
+      const int mt = static_cast<int>(cdiv(next, kBM));
+      GemmArgs a = base;
+      a.row0 = static_cast<int>(row0);
+      a.col0 = static_cast<int>(col0);
+      // dZ block = softmax - onehot for rows [row0, row0+next), cols [col0, col0+vext)
+      a.tiles_m = mt;
+      a.tiles_n = vt;
+      a.units = mt * vt;
+      a.k_blocks = static_cast<int>(cdiv(H, kBK));
+      FLCE_CUDA(launch_gemm(kKindR, t_x_k, t_w_k, a, std::min(a.units, dev.sms), s));
+      if (dX) {
+        GemmArgs b = base;
+        b.row0 = a.row0;
+        b.col0 = a.col0;
+        b.tiles_m = mt;
+        b.tiles_n = p.h_tiles;
+        b.units = mt * p.h_tiles;
+        b.k_blocks = vt * (kBN / kBK);
+        if (dx_final)
+          b.final_out = static_cast<__nv_bfloat16*>(dX);
+        else
+          b.acc = dxf;
+        FLCE_CUDA(launch_gemm(kKindX, t_dz_k, t_w_mn, b, std::min(b.units, dev.sms), s));
+      }
+      if (dW) {
+        GemmArgs c = base;
+        c.row0 = a.row0;
+        c.col0 = a.col0;
+        c.tiles_m = static_cast<int>(cdiv(vext, kBM));
+        c.tiles_n = p.h_tiles;
+        c.units = c.tiles_m * p.h_tiles;
+        c.k_blocks = mt * (kBM / kBK);
+        if (dw_final)
+          c.final_out = static_cast<__nv_bfloat16*>(dW);
+        else
+          c.acc = dwf;
+        FLCE_CUDA(launch_gemm(kKindW, t_dz_mn, t_x_mn, c, std::min(c.units, dev.sms), s));
+      }
+    }
+    if (dW && !dw_final)
+      FLCE_CUDA(launch_downcast(dwf, static_cast<__nv_bfloat16*>(dW) + col0 * H,
+                                static_cast<size_t>(vext) * H, grad_loss, nv, red, s));
+  }
+  if (dX && !dx_final)
+    FLCE_CUDA(launch_downcast(dxf, static_cast<__nv_bfloat16*>(dX), static_cast<size_t>(N) * H,
+                              grad_loss, nv, red, s));
+  return FLCE_OK;
+}
+
+flce_status flce_get_error(const void* workspace, flce_stream_t stream) {
+  if (!workspace) return FLCE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  int e = 0;
+  if (cudaMemcpy(&e, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (e & kErrTimeout) return FLCE_ERR_TIMEOUT;
+  if (e & kErrLabel) return FLCE_ERR_LABEL_OUT_OF_RANGE;
+  return FLCE_OK;
+}
+
+flce_status flce_selftest_wait_timeout(int64_t limit_ns, void* workspace, size_t workspace_bytes,
+                                       flce_stream_t stream) {
+  if (!workspace || workspace_bytes < 256 || limit_ns <= 0) return FLCE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  flce_status st = device_info(&dev);
+  if (st != FLCE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* err = static_cast<int*>(workspace);
+  FLCE_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  FLCE_CUDA(launch_selftest_wait(static_cast<unsigned long long>(limit_ns), err, s));
+  return FLCE_OK;
+}
+
+}  // extern "C"

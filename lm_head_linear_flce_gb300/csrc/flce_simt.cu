@@ -1,0 +1,193 @@
+// Small SIMT kernels around the tensor-core GEMMs: target preparation, the
+// per-row log-sum-exp merge with a deterministic loss reduction, the scaled
+// FP32 -> bf16 downcast of the gradients, and the bounded-wait self-test.
+#include "flce_device.cuh"
+#include "flce_internal.h"
+
+namespace flce {
+
+namespace {
+
+constexpr int kPrepThreads = 256;
+constexpr int kMergeThreads = 256;
+constexpr int kFinalThreads = 256;
+
+// Effective target of every row after the optional per-sequence shift (the
+// call `linear_cross_entropy(..., ignore_index=-100, shift=True, ...)` with
+// labels = input_ids in the Qwen3.5-35B-A3B LoRA SFT blog post, listings
+// `_patch_model_with_cce` and `prepare_dataset`): -1 when the row has no valid
+// target.  Counts valid rows exactly.
+__global__ void prep_targets_kernel(const int64_t* __restrict__ labels, int N, int seq_len,
+                                    int shift, int64_t ignore_index, int V,
+                                    int* __restrict__ targets, unsigned long long* n_valid,
+                                    int* err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  int ok = 0;
+  if (i < N) {
+    int64_t lab;
+    if (shift) {
+      const int pos = i % seq_len;
+      lab = (pos + 1 < seq_len) ? labels[i + 1] : ignore_index;
+    } else {
+      lab = labels[i];
+    }
+    int t = -1;
+    if (lab != ignore_index) {
+      if (lab >= 0 && lab < V) {
+        t = static_cast<int>(lab);
+        ok = 1;
+      } else {
+        atomicOr(err, kErrLabel);
+      }
+    }
+    targets[i] = t;
+  }
+  const int cnt = __syncthreads_count(ok);
+  if (n_valid && threadIdx.x == 0 && cnt) atomicAdd(n_valid, static_cast<unsigned long long>(cnt));
+}
+
+// lse_i = M + log sum_k s_k exp(m_k - M) over the forward's per-unit partials
+// (m_k, s_k); row loss = lse_i - z_{i,t_i} for valid rows.  Each block writes
+// the sum of its rows' losses (fixed tree order, FP64).
+__global__ void merge_lse_kernel(const float2* __restrict__ partials, int nchunks, int N,
+                                 const float* __restrict__ zt, const int* __restrict__ targets,
+                                 float* __restrict__ lse, double* __restrict__ loss_partials) {
+  __shared__ double red[kMergeThreads];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  double row_loss = 0.0;
+  if (i < N) {
+    float M = -INFINITY;
+    for (int k = 0; k < nchunks; ++k) M = fmaxf(M, partials[static_cast<size_t>(k) * N + i].x);
+    float S = 0.f;
+    for (int k = 0; k < nchunks; ++k) {
+      const float2 p = partials[static_cast<size_t>(k) * N + i];
+      S += p.y * expf(p.x - M);
+    }
+    const float l = M + logf(S);
+    lse[i] = l;
+    if (targets[i] >= 0) row_loss = static_cast<double>(l) - static_cast<double>(zt[i]);
+  }
+  red[threadIdx.x] = row_loss;
+  __syncthreads();
+  for (int s = kMergeThreads / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) loss_partials[blockIdx.x] = red[0];
+}
+
+// Sum of the block partials in a fixed order; mean divides by n_valid
+// (0 when there is no valid target).
+__global__ void finalize_loss_kernel(const double* __restrict__ loss_partials, int nblocks,
+                                     const long long* __restrict__ n_valid, int reduction,
+                                     float* __restrict__ loss) {
+  __shared__ double red[kFinalThreads];
+  double acc = 0.0;
+  for (int b = threadIdx.x; b < nblocks; b += kFinalThreads) acc += loss_partials[b];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = kFinalThreads / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    double v = red[0];
+    if (reduction == 0) {
+      const long long n = *n_valid;
+      v = n > 0 ? v / static_cast<double>(n) : 0.0;
+    }
+    *loss = static_cast<float>(v);
+  }
+}
+
+// dst = bf16_rn(scale * src), scale = g / n_valid (mean) or g (sum): the FP32
+// buffer is rounded to bf16 once, after accumulation (Megatron-LM PR #2739,
+// section 2).  Eight elements per thread; count is a multiple of 8.
+__global__ void downcast_kernel(const float4* __restrict__ src, uint4* __restrict__ dst,
+                                size_t count8, const float* __restrict__ grad_loss,
+                                const long long* __restrict__ n_valid, int reduction) {
+  float scale = *grad_loss;
+  if (reduction == 0) {
+    const long long n = *n_valid;
+    scale = n > 0 ? scale / static_cast<float>(n) : 0.f;
+  }
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < count8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 a = src[2 * i], b = src[2 * i + 1];
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(scale * a.x, scale * a.y);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(scale * a.z, scale * a.w);
+    __nv_bfloat162 p2 = __floats2bfloat162_rn(scale * b.x, scale * b.y);
+    __nv_bfloat162 p3 = __floats2bfloat162_rn(scale * b.z, scale * b.w);
+    dst[i] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                        *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+  }
+}
+
+// Waits on a barrier that nothing will ever complete; the bounded wait must
+// give up, record the timeout and let the kernel return.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0u;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    WaitCtx w{&abort_flag, err, limit_ns};
+    wait_parity(smem_u32(&bar), 0u, w);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int shift,
+                                int64_t ignore_index, int V, int* targets, long long* n_valid,
+                                int* err, cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  const int blocks = (N + kPrepThreads - 1) / kPrepThreads;
+  prep_targets_kernel<<<blocks, kPrepThreads, 0, st>>>(
+      labels, N, seq_len, shift, ignore_index, V, targets,
+      reinterpret_cast<unsigned long long*>(n_valid), err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_lse(const float2* partials, int nchunks, int N, const float* zt,
+                             const int* targets, float* lse, double* loss_partials,
+                             cudaStream_t st, int* nblocks_out) {
+  const int blocks = (N + kMergeThreads - 1) / kMergeThreads;
+  *nblocks_out = blocks;
+  if (blocks == 0) return cudaSuccess;
+  merge_lse_kernel<<<blocks, kMergeThreads, 0, st>>>(partials, nchunks, N, zt, targets, lse,
+                                                     loss_partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_loss(const double* loss_partials, int nblocks,
+                                 const long long* n_valid, int reduction, float* loss,
+                                 cudaStream_t st) {
+  finalize_loss_kernel<<<1, kFinalThreads, 0, st>>>(loss_partials, nblocks, n_valid, reduction,
+                                                    loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_downcast(const float* src, __nv_bfloat16* dst, size_t count,
+                            const float* grad_loss, const long long* n_valid, int reduction,
+                            cudaStream_t st) {
+  const size_t count8 = count / 8;
+  if (count8 == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t want = (count8 + 255) / 256;
+  const int blocks = static_cast<int>(want < static_cast<size_t>(sms) * 8 ? want : sms * 8);
+  downcast_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(src),
+                                          reinterpret_cast<uint4*>(dst), count8, grad_loss,
+                                          n_valid, reduction);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* err, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

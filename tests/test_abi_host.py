@@ -1,0 +1,104 @@
+"""The C ABI without a GPU: the library loads, exports every symbol declared in
+include/flce.h, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+
+flce = pytest.importorskip("lm_head_linear_flce_gb300")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(flce.library_path):
+        from lm_head_linear_flce_gb300 import _build
+        _build.build()
+    return flce.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flce_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("flce_workspace_size", "flce_forward", "flce_backward", "flce_get_error",
+                 "flce_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in flce.STATUS.items():
+        assert lib.flce_status_string(code).decode() == name
+
+
+def test_workspace_size_is_bounded(lib):
+    # O(N*H + Vb*H + N*V/1024), far below the N x V logits it replaces
+    for N, H, V in [(8192, 3584, 152064), (32768, 2048, 151936), (4096, 8192, 128256),
+                    (16384, 4096, 151936), (256, 256, 4096)]:
+        ws = lib.flce_workspace_size(N, H, V)
+        assert ws > 0
+        assert ws < 0.2 * N * V * 2 + (N + 8192) * H * 4 + 64 * 2**20, (N, H, V, ws)
+    assert lib.flce_workspace_size(8, 12, 100) == 0     # H % 8 != 0
+    assert lib.flce_workspace_size(8, 0, 100) == 0
+    assert lib.flce_workspace_size(-1, 64, 100) == 0
+    assert lib.flce_workspace_size(0, 64, 100) > 0      # an empty batch is allowed
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def test_forward_rejects_bad_arguments_on_host(lib):
+    ws_need = lib.flce_workspace_size(64, 64, 100)
+    args = dict(X=_fake(), W=_fake(), labels=_fake(), N=64, H=64, V=100, seq_len=0,
+                ignore=-100, shift=0, red=0, loss=_fake(), lse=_fake(), nv=_fake(),
+                ws=_fake(0x100000), wsb=ws_need, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.flce_forward(a["X"], a["W"], a["labels"], a["N"], a["H"], a["V"],
+                                a["seq_len"], a["ignore"], a["shift"], a["red"], a["loss"],
+                                a["lse"], a["nv"], a["ws"], a["wsb"], a["stream"])
+
+    assert call(X=None) == 1
+    assert call(H=12) == 2
+    assert call(V=0) == 1
+    assert call(red=7) == 1
+    assert call(wsb=ws_need - 1) == 3
+    assert call(ws=_fake(0x100010)) == 1               # workspace not 256-byte aligned
+    assert call(X=_fake(0x10008)) == 1                 # X not 16-byte aligned
+    assert call(shift=1, seq_len=48) == 1              # N % seq_len != 0
+
+
+def test_backward_rejects_bad_arguments_on_host(lib):
+    ws_need = lib.flce_workspace_size(64, 64, 100)
+    f = lib.flce_backward
+    base = [_fake(), _fake(), _fake(), 64, 64, 100, 0, -100, 0, 0, _fake(), _fake(), _fake(),
+            _fake(), _fake(), _fake(0x100000), ws_need, None]
+    assert f(*base[:12], None, *base[13:]) == 1       # no grad_loss
+    b = list(base)
+    b[16] = ws_need - 256
+    assert f(*b) == 3
+
+
+def test_plan_blocks_follow_the_tuning_knob(lib):
+    a = lib.flce_workspace_size(4096, 1024, 50000)
+    lib.flce_set_backward_block(128, 128 * 256)
+    try:
+        b = lib.flce_workspace_size(4096, 1024, 50000)
+    finally:
+        lib.flce_set_backward_block(0, 0)
+    assert lib.flce_workspace_size(4096, 1024, 50000) == a
+    assert b != a
