@@ -1,0 +1,364 @@
+"""Throughput of the fused linear cross-entropy (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qwen2_7b]
+                    [--impl ours|reference]
+
+One step is flce_forward + flce_backward (loss, lse, n_valid, dX, dW) over one
+batch of the workload, inputs resident in HBM.  The workload's weight matrix
+alone (V x H bf16, >= 1 GB) is larger than the 129 MB L2, so no flush is
+needed between steps.  Prints one JSON line (rank 0).
+
+--impl reference times the CPU float64 oracle on the host cores instead (a
+bounded sample of rows per step), reported in the same metric and unit.
+
+With several ranks (torchrun) every rank runs its own replica of the workload
+on its own GPU ("replicas only": the method has no exchange step here); value
+is the tokens of all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "fused linear-CE fwd+bwd tokens/s and TFLOP/s (% bf16 peak), peak extra HBM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    """Maximum of x over all ranks (identity for one rank)."""
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(tokens_per_step: int, steps: int, elapsed_ms_local: float, world: int,
+                         device) -> tuple[float, float]:
+    """(value, max elapsed ms): tokens of all ranks over the slowest rank's time."""
+    worst = reduce_max(elapsed_ms_local, world, device)
+    return world * tokens_per_step * steps / (worst / 1e3), worst
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "-i", str(self.gpu),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import lm_head_linear_flce_gb300 as flce
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = workloads.get(args.workload)
+    N, H, V = wl.N, wl.H, wl.V
+    Xh, Wh, Lh = workloads.make_inputs(wl)
+    Xh, Wh, Lh = Xh.pin_memory(), Wh.pin_memory(), Lh.pin_memory()
+    X, W, L = Xh.to(dev), Wh.to(dev), Lh.to(dev)
+    kw = dict(seq_len=wl.S, shift=wl.shift, reduction=wl.reduction)
+    grad = torch.ones(1, dtype=torch.float32, device=dev)
+    dX = torch.empty_like(X)
+    dW = torch.empty_like(W)
+    ws = torch.empty(flce.workspace_size(N, H, V), dtype=torch.uint8, device=dev)
+
+    def step():
+        loss, lse, nv, _ = flce.flce_forward(X, W, L, workspace=ws, **kw)
+        flce.flce_backward(X, W, L, lse, nv, grad, workspace=ws, dX=dX, dW=dW, **kw)
+        return loss
+
+    # peak extra device memory of one step: everything beyond inputs and outputs
+    torch.cuda.synchronize()
+    del ws
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    ws = torch.empty(flce.workspace_size(N, H, V), dtype=torch.uint8, device=dev)
+    loss = step()
+    torch.cuda.synchronize()
+    out_bytes = 4 + N * 4 + 8  # loss, lse, n_valid (dX, dW were allocated before `base`)
+    extra = torch.cuda.max_memory_allocated(dev) - base - out_bytes
+
+    for _ in range(args.warmup):
+        step()
+    if flce.flce_get_error(ws) != 0:
+        raise RuntimeError(f"device error after warm-up: {flce.STATUS[flce.flce_get_error(ws)]}")
+
+    stream = torch.cuda.current_stream(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    flce.flce_profile_collect()
+    flce.flce_profile_enable(True)
+    n0 = flce.flce_kernel_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    launches = flce.flce_kernel_launch_count() - n0
+    flce.flce_profile_enable(False)
+    prof = flce.flce_profile_collect()
+    status = flce.flce_get_error(ws)
+    if status != 0:
+        raise RuntimeError(f"device error in timed region: {flce.STATUS[status]}")
+    elapsed = t0.elapsed_time(t1)
+    value, worst = aggregate_throughput(N, args.steps, elapsed, world, dev)
+    ms_step = worst / args.steps
+
+    # end to end through the public autograd call, inputs from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        Xd = torch.empty_like(X)
+        Wd = torch.empty_like(W)
+        Ld = torch.empty_like(L)
+        loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+        e_steps = max(1, min(args.steps, 5))
+
+        def e2e_step():
+            Xd.copy_(Xh, non_blocking=True)
+            Wd.copy_(Wh, non_blocking=True)
+            Ld.copy_(Lh, non_blocking=True)
+            xg = Xd.detach().requires_grad_(True)
+            wg = Wd.detach().requires_grad_(True)
+            lo = flce.linear_cross_entropy(xg, wg, Ld, shift=wl.shift, reduction=wl.reduction,
+                                           seq_len=wl.S)
+            lo.backward()
+            loss_h.copy_(lo.detach().reshape(1), non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_val, _ = aggregate_throughput(N, e_steps, e0.elapsed_time(e1), world, dev)
+        h2d = X.numel() * 2 + W.numel() * 2 + L.numel() * 8
+        e2e = {"value": e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": 4, "steps": e_steps,
+               "api": "lm_head_linear_flce_gb300.linear_cross_entropy + backward"}
+
+    peaks, src = load_peaks()
+    flops = wl.flops
+    tflops = flops / (ms_step / 1e3) / 1e12 * 1.0
+    tflops_all = world * tflops
+    # dominant tensor-core kernel of the step
+    kinds = {k: v for k, v in prof.items() if v[1] > 0}
+    dom = max(kinds, key=lambda k: kinds[k][0])
+    dom_ms, dom_n = kinds[dom]
+    flops_per_step_kind = 2 * N * H * V  # each kind does one 2NHV contraction per step
+    achieved = flops_per_step_kind * args.steps / (dom_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    step_ms_total = sum(v[0] for v in kinds.values())
+    roofline = {
+        "kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+        "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+        "peak_source": f"bf16_tflops_sustained ({src})",
+        "launches_per_step": dom_n / args.steps,
+        "avg_launch_ms": dom_ms / dom_n,
+        "share_of_step": round(dom_ms / (ms_step * args.steps), 4),
+        "per_kind_ms_per_step": {k: round(v[0] / args.steps, 3) for k, v in kinds.items()},
+        "per_kind_tflops": {k: round(flops_per_step_kind * args.steps / (v[0] / 1e3) / 1e12, 1)
+                            for k, v in kinds.items()},
+        "tensor_kernels_ms_per_step": round(step_ms_total / args.steps, 3),
+    }
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, Xh, Wh, Lh, rows=args.cpu_rows)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "N": N, "H": H, "V": V, "B": wl.B, "seq_len": wl.S,
+                   "shift": wl.shift, "reduction": wl.reduction,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * H * 2 / 1e9)},
+        "tflops": round(tflops_all, 1),
+        "pct_bf16_peak": round(100 * tflops / peak, 2),
+        "pct_bf16_peak_basis": f"bf16_tflops_sustained {peak} ({src}), 8*N*H*V per step",
+        "peak_extra_hbm_bytes": int(extra),
+        "logits_bytes_avoided": {"bf16": N * V * 2, "fp32": N * V * 4},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "loss": float(loss.item()),
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ---------------------------------------------------------------- CPU oracle
+def cpu_baseline(wl, X, W, L, rows: int):
+    """The float64 oracle, as it stands, on the host cores: forward + backward of
+    `rows` token rows of the workload (their full vocabulary of logits, their dX
+    rows and their contribution to dW)."""
+    import numpy as np
+
+    import oracle
+    t, valid, n_valid, _ = oracle.effective_targets(L, wl.V, seq_len=wl.S, shift=wl.shift)
+    idx = np.arange(rows) * max(1, wl.N // rows)
+    tgt = torch.tensor(np.where(valid[idx], t[idx], -100))
+    Xs = X[torch.as_tensor(idx)]
+    t0 = time.perf_counter()
+    f = oracle.forward(Xs, W, tgt, reduction=wl.reduction)
+    oracle.backward(Xs, W, tgt, reduction="sum",
+                    grad_loss=(1.0 / n_valid if wl.reduction == "mean" else 1.0), lse=f["lse"])
+    dt = time.perf_counter() - t0
+    return {"value": round(rows / dt, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{rows} token rows of {wl.name} (every {max(1, wl.N // rows)}th), "
+                      "float64 forward + backward incl. their dW contribution"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    wl = workloads.get(args.workload)
+    X, W, L = workloads.make_inputs(wl)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        cpu_baseline(wl, X, W, L, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cb = cpu_baseline(wl, X, W, L, rows)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    res = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * dt / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "N": wl.N, "H": wl.H, "V": wl.V, "B": wl.B,
+                   "seq_len": wl.S, "shift": wl.shift, "reduction": wl.reduction,
+                   "parallelism": "single"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": cb["sample"]},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--workload", default="qwen2_7b", choices=sorted(workloads.BY_NAME))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-rows", type=int, default=384)
+    p.add_argument("--ref-rows", type=int, default=8)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1 and torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -146,6 +146,24 @@ void flce_set_wait_limit_ns(int64_t limit_ns);
 void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems);
 
 /*
+ * Measurement hooks.
+ *
+ * flce_kernel_launch_count: kernels this library has launched in this process
+ * (tensor-core GEMMs and the small SIMT kernels; memsets not included).
+ *
+ * flce_profile_enable(1) makes every later tensor-core kernel launch record a
+ * CUDA event on the launching stream just before and just after it (events
+ * come from a pool the library owns; no device memory is allocated).
+ * flce_profile_collect waits for those events, writes per-kind totals into
+ * ms[4] and launches[4] (index 0: forward GEMM + log-sum-exp, 1: dZ
+ * recompute, 2: dX contraction, 3: dW contraction), clears the records and
+ * returns FLCE_OK, or FLCE_ERR_CUDA.  flce_profile_enable(0) stops recording.
+ */
+int64_t flce_kernel_launch_count(void);
+void flce_profile_enable(int enable);
+flce_status flce_profile_collect(double* ms, int64_t* launches);
+
+/*
  * Self-test of the bounded-wait path: enqueues one small kernel that waits on
  * a barrier nothing will ever complete, with a limit of `limit_ns`, then
  * records FLCE_ERR_TIMEOUT in the workspace error word and returns cleanly.

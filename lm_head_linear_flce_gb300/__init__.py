@@ -21,7 +21,8 @@ import torch
 __all__ = [
     "FlceError", "library", "library_path", "workspace_size", "flce_forward", "flce_backward",
     "flce_get_error", "flce_selftest_wait_timeout", "flce_set_wait_limit_ns",
-    "flce_set_backward_block",
+    "flce_set_backward_block", "flce_kernel_launch_count", "flce_profile_enable",
+    "flce_profile_collect", "PROFILE_KINDS",
     "linear_cross_entropy", "STATUS",
 ]
 
@@ -73,6 +74,12 @@ def library() -> ctypes.CDLL:
     lib.flce_set_wait_limit_ns.restype = None
     lib.flce_set_backward_block.argtypes = [c_i64, c_i64]
     lib.flce_set_backward_block.restype = None
+    lib.flce_kernel_launch_count.argtypes = []
+    lib.flce_kernel_launch_count.restype = c_i64
+    lib.flce_profile_enable.argtypes = [c_int]
+    lib.flce_profile_enable.restype = None
+    lib.flce_profile_collect.argtypes = [c_p, c_p]
+    lib.flce_profile_collect.restype = c_int
     lib.flce_selftest_wait_timeout.argtypes = [c_i64, c_p, c_sz, c_p]
     lib.flce_selftest_wait_timeout.restype = c_int
     _lib = lib
@@ -174,6 +181,28 @@ def flce_set_wait_limit_ns(limit_ns: int) -> None:
 def flce_set_backward_block(max_rows: int = 0, max_block_elems: int = 0) -> None:
     """Caps the backward's dZ block (0 restores the defaults); see include/flce.h."""
     library().flce_set_backward_block(int(max_rows), int(max_block_elems))
+
+
+def flce_kernel_launch_count() -> int:
+    return int(library().flce_kernel_launch_count())
+
+
+def flce_profile_enable(enable: bool) -> None:
+    library().flce_profile_enable(int(bool(enable)))
+
+
+PROFILE_KINDS = ("forward_lse", "dz_recompute", "dx_contraction", "dw_contraction")
+
+
+def flce_profile_collect() -> dict:
+    """{kind: (total_ms, launches)} of the tensor-core launches recorded since
+    profiling was enabled or last collected; waits for them to finish."""
+    ms = (ctypes.c_double * 4)()
+    n = (ctypes.c_int64 * 4)()
+    _check(library().flce_profile_collect(ctypes.cast(ms, ctypes.c_void_p),
+                                          ctypes.cast(n, ctypes.c_void_p)),
+           "flce_profile_collect")
+    return {k: (ms[i], int(n[i])) for i, k in enumerate(PROFILE_KINDS)}
 
 
 def flce_selftest_wait_timeout(limit_ns: int, workspace) -> int:

@@ -7,6 +7,8 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "../../include/flce.h"
 #include "flce_internal.h"
@@ -112,12 +114,49 @@ flce_status check_common(const void* X, const void* W, const int64_t* labels, in
   return FLCE_OK;
 }
 
+// ------------------------------------------------------------ measurement
+std::atomic<int64_t> g_launches{0};
+std::atomic<bool> g_prof_on{false};
+std::mutex g_prof_mu;
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launches one tensor-core kernel, bracketed by profiling events when enabled.
+cudaError_t gemm(GemmKind kind, const CUtensorMap& ta, const CUtensorMap& tb,
+                 const GemmArgs& a, int grid, cudaStream_t s) {
+  if (!g_prof_on.load()) return launch_gemm(kind, ta, tb, a, grid, s);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  ProfRec r{static_cast<int>(kind), take_event(), take_event()};
+  if (r.a) cudaEventRecord(r.a, s);
+  cudaError_t e = launch_gemm(kind, ta, tb, a, grid, s);
+  if (r.b) cudaEventRecord(r.b, s);
+  if (r.a && r.b) g_prof.push_back(r);
+  return e;
+}
+
 #define FLCE_CUDA(x)                         \
   do {                                       \
     if ((x) != cudaSuccess) return FLCE_ERR_CUDA; \
   } while (0)
 
 }  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   if (N < 0 || H <= 0 || V <= 0) return false;
@@ -259,7 +298,7 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   a.zt = zt;
   a.err = err;
   a.wait_limit_ns = g_wait_limit_ns.load();
-  FLCE_CUDA(launch_gemm(kKindFwd, tx, tw, a, std::min(a.units, dev.sms), s));
+  FLCE_CUDA(gemm(kKindFwd, tx, tw, a, std::min(a.units, dev.sms), s));
   int nblocks = 0;
   FLCE_CUDA(launch_merge_lse(part, p.v_units, static_cast<int>(N), zt, targets, lse, lossp, s,
                              &nblocks));
@@ -348,7 +387,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
       a.tiles_n = vt;
       a.units = mt * vt;
       a.k_blocks = static_cast<int>(cdiv(H, kBK));
-      FLCE_CUDA(launch_gemm(kKindR, t_x_k, t_w_k, a, std::min(a.units, dev.sms), s));
+      FLCE_CUDA(gemm(kKindR, t_x_k, t_w_k, a, std::min(a.units, dev.sms), s));
       if (dX) {
         GemmArgs b = base;
         b.row0 = a.row0;
@@ -361,7 +400,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
           b.final_out = static_cast<__nv_bfloat16*>(dX);
         else
           b.acc = dxf;
-        FLCE_CUDA(launch_gemm(kKindX, t_dz_k, t_w_mn, b, std::min(b.units, dev.sms), s));
+        FLCE_CUDA(gemm(kKindX, t_dz_k, t_w_mn, b, std::min(b.units, dev.sms), s));
       }
       if (dW) {
         GemmArgs c = base;
@@ -375,7 +414,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
           c.final_out = static_cast<__nv_bfloat16*>(dW);
         else
           c.acc = dwf;
-        FLCE_CUDA(launch_gemm(kKindW, t_dz_mn, t_x_mn, c, std::min(c.units, dev.sms), s));
+        FLCE_CUDA(gemm(kKindW, t_dz_mn, t_x_mn, c, std::min(c.units, dev.sms), s));
       }
     }
     if (dW && !dw_final)
@@ -398,6 +437,32 @@ flce_status flce_get_error(const void* workspace, flce_stream_t stream) {
   if (e & kErrTimeout) return FLCE_ERR_TIMEOUT;
   if (e & kErrLabel) return FLCE_ERR_LABEL_OUT_OF_RANGE;
   return FLCE_OK;
+}
+
+int64_t flce_kernel_launch_count(void) { return g_launches.load(); }
+
+void flce_profile_enable(int enable) { g_prof_on.store(enable != 0); }
+
+flce_status flce_profile_collect(double* ms, int64_t* launches) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (int k = 0; k < 4; ++k) {
+    if (ms) ms[k] = 0.0;
+    if (launches) launches[k] = 0;
+  }
+  flce_status st = FLCE_OK;
+  for (const ProfRec& r : g_prof) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      st = FLCE_ERR_CUDA;
+    if (r.kind >= 0 && r.kind < 4) {
+      if (ms) ms[r.kind] += t;
+      if (launches) launches[r.kind] += 1;
+    }
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  return st;
 }
 
 flce_status flce_selftest_wait_timeout(int64_t limit_ns, void* workspace, size_t workspace_bytes,

@@ -479,6 +479,7 @@ cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& ta, const CUtensorMap&
     case kKindW: FLCE_LAUNCH(kKindW); break;
   }
 #undef FLCE_LAUNCH
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -77,6 +77,9 @@ struct Plan {
 
 bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p);
 
+// Counts one kernel launch (see flce_kernel_launch_count).
+void note_launch();
+
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int shift,
                                 int64_t ignore_index, int V, int* targets,

@@ -147,6 +147,7 @@ cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int s
   prep_targets_kernel<<<blocks, kPrepThreads, 0, st>>>(
       labels, N, seq_len, shift, ignore_index, V, targets,
       reinterpret_cast<unsigned long long*>(n_valid), err);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -158,6 +159,7 @@ cudaError_t launch_merge_lse(const float2* partials, int nchunks, int N, const f
   if (blocks == 0) return cudaSuccess;
   merge_lse_kernel<<<blocks, kMergeThreads, 0, st>>>(partials, nchunks, N, zt, targets, lse,
                                                      loss_partials);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -166,6 +168,7 @@ cudaError_t launch_finalize_loss(const double* loss_partials, int nblocks,
                                  cudaStream_t st) {
   finalize_loss_kernel<<<1, kFinalThreads, 0, st>>>(loss_partials, nblocks, n_valid, reduction,
                                                     loss);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -182,11 +185,13 @@ cudaError_t launch_downcast(const float* src, __nv_bfloat16* dst, size_t count,
   downcast_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(src),
                                           reinterpret_cast<uint4*>(dst), count8, grad_loss,
                                           n_valid, reduction);
+  note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* err, cudaStream_t st) {
   selftest_wait_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+  note_launch();
   return cudaGetLastError();
 }
 
