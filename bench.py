@@ -135,6 +135,12 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = workloads.get(args.workload)
+    if args.tokens or args.vocab:
+        # a reduced case of the same workload (profiling captures)
+        import dataclasses
+        n = args.tokens or wl.N
+        wl = dataclasses.replace(wl, name=f"{wl.name}_N{n}_V{args.vocab or wl.V}", B=1, S=n,
+                                 V=args.vocab or wl.V)
     N, H, V = wl.N, wl.H, wl.V
     Xh, Wh, Lh = workloads.make_inputs(wl)
     Xh, Wh, Lh = Xh.pin_memory(), Wh.pin_memory(), Lh.pin_memory()
@@ -346,6 +352,8 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-rows", type=int, default=384)
     p.add_argument("--ref-rows", type=int, default=8)
+    p.add_argument("--tokens", type=int, default=0, help="override N (profiling cases)")
+    p.add_argument("--vocab", type=int, default=0, help="override V (profiling cases)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
