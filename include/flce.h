@@ -173,6 +173,36 @@ flce_status flce_profile_collect(double* ms, int64_t* launches);
 flce_status flce_selftest_wait_timeout(int64_t limit_ns, void* workspace,
                                        size_t workspace_bytes, flce_stream_t stream);
 
+/*
+ * flce_forward with no workspace: for callers that cannot allocate device
+ * memory (code running inside a host framework that owns every device
+ * allocation and passes in only input and output buffers, or a path where the
+ * device-synchronising cudaMalloc / cudaFree are not allowed).  The pages have
+ * no counterpart: this is a deployment variant of flce_forward, same kernels,
+ * same results.
+ *
+ *   Arguments as in flce_forward, minus the workspace.
+ *   device_error    device int, 1 element, or NULL: receives this call's
+ *                   device error bits (0 none, 1 label out of range, 2 wait
+ *                   timeout).
+ * The scratch is a fixed 16 MiB array in the library's device image (held by
+ * every GPU that loads the library until the process exits); it fits
+ *   16 + 8*N + 8*N*ceil(V/1024) + 8*(N/256 + 2) bytes (each term rounded up to
+ *   256): e.g. N = 8192 at V = 152064.
+ * Larger problems are rejected with FLCE_ERR_WORKSPACE_TOO_SMALL before
+ * anything is enqueued.  Allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library call.  The first call on a device looks up the scratch
+ * address there (cudaGetSymbolAddress); make that first call before any stream
+ * capture on that device.  All calls share the scratch and it keeps the last
+ * call's contents (each call clears what must start at zero); calls whose work
+ * overlaps on the GPU race on it, so serialise them (one stream, or events).
+ */
+flce_status flce_forward_noalloc(const void* X, const void* W, const int64_t* labels,
+                                 int64_t N, int64_t H, int64_t V, int64_t seq_len,
+                                 int64_t ignore_index, int shift, flce_reduction reduction,
+                                 float* loss, float* lse, int64_t* n_valid, int* device_error,
+                                 flce_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

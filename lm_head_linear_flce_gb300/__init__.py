@@ -22,7 +22,7 @@ __all__ = [
     "FlceError", "library", "library_path", "workspace_size", "flce_forward", "flce_backward",
     "flce_get_error", "flce_selftest_wait_timeout", "flce_set_wait_limit_ns",
     "flce_set_backward_block", "flce_kernel_launch_count", "flce_profile_enable",
-    "flce_profile_collect", "PROFILE_KINDS",
+    "flce_profile_collect", "PROFILE_KINDS", "flce_forward_noalloc",
     "linear_cross_entropy", "STATUS",
 ]
 
@@ -209,6 +209,36 @@ def flce_selftest_wait_timeout(limit_ns: int, workspace) -> int:
     return int(library().flce_selftest_wait_timeout(int(limit_ns), _ptr(workspace),
                                                     workspace.numel(),
                                                     _stream(workspace.device)))
+
+
+def flce_forward_noalloc(X, W, labels, *, seq_len=None, ignore_index=-100, shift=False,
+                         reduction="mean"):
+    """flce_forward without a workspace (C entry point flce_forward_noalloc).
+
+    For callers that cannot allocate device memory: the library keeps a fixed
+    16 MiB scratch array in its device image and uses it instead.  Returns
+    (loss [1] f32, lse [N] f32, n_valid [1] i64, device_error [1] i32).  Calls
+    share the scratch; serialise calls that could overlap on the GPU.
+    """
+    _check_inputs(X, W, labels)
+    lib = library()
+    fn = lib.flce_forward_noalloc
+    c_i64, c_p, c_int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i64, c_i64, c_int, c_int,
+                   c_p, c_p, c_p, c_p, c_p]
+    fn.restype = c_int
+    N, H = X.shape
+    V = W.shape[0]
+    dev = X.device
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    derr = torch.empty(1, dtype=torch.int32, device=dev)
+    st = fn(_ptr(X), _ptr(W), _ptr(labels), N, H, V, int(seq_len or 0), int(ignore_index),
+            int(bool(shift)), _REDUCTION[reduction], _ptr(loss), _ptr(lse), _ptr(n_valid),
+            _ptr(derr), _stream(dev))
+    _check(st, "flce_forward_noalloc")
+    return loss, lse, n_valid, derr
 
 
 class _FusedLinearCE(torch.autograd.Function):
