@@ -239,12 +239,13 @@ def run_ours(args, world, rank, local):
     flops = wl.flops
     tflops = flops / (ms_step / 1e3) / 1e12 * 1.0
     tflops_all = world * tflops
-    # dominant tensor-core kernel of the step
+    # dominant tensor-core kernel of the step: forward launch (2NHV) or the
+    # backward launches (recompute + dX + dW, 6NHV)
+    kind_flops = {"forward": 2 * N * H * V, "backward": 6 * N * H * V}
     kinds = {k: v for k, v in prof.items() if v[1] > 0}
     dom = max(kinds, key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
-    flops_per_step_kind = 2 * N * H * V  # each kind does one 2NHV contraction per step
-    achieved = flops_per_step_kind * args.steps / (dom_ms / 1e3) / 1e12
+    achieved = kind_flops[dom] * args.steps / (dom_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     step_ms_total = sum(v[0] for v in kinds.values())
     roofline = {
@@ -253,9 +254,10 @@ def run_ours(args, world, rank, local):
         "peak_source": f"bf16_tflops_sustained ({src})",
         "launches_per_step": dom_n / args.steps,
         "avg_launch_ms": dom_ms / dom_n,
+        "flops_per_launch": kind_flops[dom] * args.steps / dom_n,
         "share_of_step": round(dom_ms / (ms_step * args.steps), 4),
         "per_kind_ms_per_step": {k: round(v[0] / args.steps, 3) for k, v in kinds.items()},
-        "per_kind_tflops": {k: round(flops_per_step_kind * args.steps / (v[0] / 1e3) / 1e12, 1)
+        "per_kind_tflops": {k: round(kind_flops[k] * args.steps / (v[0] / 1e3) / 1e12, 1)
                             for k, v in kinds.items()},
         "tensor_kernels_ms_per_step": round(step_ms_total / args.steps, 3),
     }

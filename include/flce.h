@@ -155,9 +155,10 @@ void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems);
  * CUDA event on the launching stream just before and just after it (events
  * come from a pool the library owns; no device memory is allocated).
  * flce_profile_collect waits for those events, writes per-kind totals into
- * ms[4] and launches[4] (index 0: forward GEMM + log-sum-exp, 1: dZ
- * recompute, 2: dX contraction, 3: dW contraction), clears the records and
- * returns FLCE_OK, or FLCE_ERR_CUDA.  flce_profile_enable(0) stops recording.
+ * ms[4] and launches[4] (index 0: forward GEMM with its log-sum-exp epilogue,
+ * 1: backward GEMM launches, each holding dZ-recompute, dX and dW tiles;
+ * 2 and 3 are reserved and stay 0), clears the records and returns FLCE_OK,
+ * or FLCE_ERR_CUDA.  flce_profile_enable(0) stops recording.
  */
 int64_t flce_kernel_launch_count(void);
 void flce_profile_enable(int enable);

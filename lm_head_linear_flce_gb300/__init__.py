@@ -191,7 +191,7 @@ def flce_profile_enable(enable: bool) -> None:
     library().flce_profile_enable(int(bool(enable)))
 
 
-PROFILE_KINDS = ("forward_lse", "dz_recompute", "dx_contraction", "dw_contraction")
+PROFILE_KINDS = ("forward", "backward")
 
 
 def flce_profile_collect() -> dict:

@@ -136,14 +136,14 @@ cudaEvent_t take_event() {
   return e;
 }
 
-// Launches one tensor-core kernel, bracketed by profiling events when enabled.
-cudaError_t gemm(GemmKind kind, const CUtensorMap& ta, const CUtensorMap& tb,
-                 const GemmArgs& a, int grid, cudaStream_t s) {
-  if (!g_prof_on.load()) return launch_gemm(kind, ta, tb, a, grid, s);
+// Brackets one tensor-core launch with profiling events when enabled.
+template <class F>
+cudaError_t profiled(int kind, cudaStream_t s, F&& launch) {
+  if (!g_prof_on.load()) return launch();
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  ProfRec r{static_cast<int>(kind), take_event(), take_event()};
+  ProfRec r{kind, take_event(), take_event()};
   if (r.a) cudaEventRecord(r.a, s);
-  cudaError_t e = launch_gemm(kind, ta, tb, a, grid, s);
+  cudaError_t e = launch();
   if (r.b) cudaEventRecord(r.b, s);
   if (r.a && r.b) g_prof.push_back(r);
   return e;
@@ -201,13 +201,16 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   off = align_up(off + static_cast<size_t>(cdiv(N, 256) + 1) * 8);
   const size_t fwd_end = off;
   // backward view (overlaps the forward view: the workspace need not persist)
+  p->launches = p->n_blocks * p->v_blocks + 1;
   off = shared_start;
+  p->off_cnt = off;
+  off = align_up(off + static_cast<size_t>(p->launches) * 4);
   p->off_dxf = off;
   if (p->v_blocks > 1) off = align_up(off + static_cast<size_t>(N) * H * 4);
   p->off_dwf = off;
   if (p->multi_n) off = align_up(off + static_cast<size_t>(p->Vb) * H * 4);
-  p->off_dz = off;
-  off = align_up(off + static_cast<size_t>(p->Nb) * p->Vb * 2);
+  p->off_dz = off;  // two slots: block p is formed while block p-1 is consumed
+  off = align_up(off + 2 * static_cast<size_t>(p->Nb) * p->Vb * 2);
   p->total = std::max(fwd_end, off);
   return true;
 }
@@ -298,7 +301,7 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   a.zt = zt;
   a.err = err;
   a.wait_limit_ns = g_wait_limit_ns.load();
-  FLCE_CUDA(gemm(kKindFwd, tx, tw, a, std::min(a.units, dev.sms), s));
+  FLCE_CUDA(profiled(0, s, [&] { return launch_fwd_gemm(tx, tw, a, std::min(a.units, dev.sms), s); }));
   int nblocks = 0;
   FLCE_CUDA(launch_merge_lse(part, p.v_units, static_cast<int>(N), zt, targets, lse, lossp, s,
                              &nblocks));
@@ -339,87 +342,99 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
 
   float* dxf = reinterpret_cast<float*>(ws + p.off_dxf);
   float* dwf = reinterpret_cast<float*>(ws + p.off_dwf);
-  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + p.off_dz);
+  int* counters = reinterpret_cast<int*>(ws + p.off_cnt);
+  __nv_bfloat16* dz0 = reinterpret_cast<__nv_bfloat16*>(ws + p.off_dz);
+  __nv_bfloat16* dz1 = dz0 + static_cast<size_t>(p.Nb) * p.Vb;
   const bool dx_final = p.v_blocks == 1;
   const bool dw_final = !p.multi_n;
+  FLCE_CUDA(cudaMemsetAsync(counters, 0, static_cast<size_t>(p.launches) * 4, s));
   if (dX && !dx_final) FLCE_CUDA(cudaMemsetAsync(dxf, 0, static_cast<size_t>(N) * H * 4, s));
 
-  CUtensorMap t_x_k, t_w_k, t_dz_k, t_w_mn, t_dz_mn, t_x_mn;
-  if (!make_tmap(&t_x_k, X, H, N, H * 2, kBK, kBM) ||
-      !make_tmap(&t_w_k, W, H, V, H * 2, kBK, kBN) ||
-      !make_tmap(&t_dz_k, dz, p.Vb, p.Nb, p.Vb * 2, kBK, kBM) ||
-      !make_tmap(&t_w_mn, W, H, V, H * 2, 64, 64) ||
-      !make_tmap(&t_dz_mn, dz, p.Vb, p.Nb, p.Vb * 2, 64, 64) ||
-      !make_tmap(&t_x_mn, X, H, N, H * 2, 64, 64))
+  BwdMaps maps;
+  if (!make_tmap(&maps.x_k, X, H, N, H * 2, kBK, kBM) ||
+      !make_tmap(&maps.w_k, W, H, V, H * 2, kBK, kBN) ||
+      !make_tmap(&maps.w_mn, W, H, V, H * 2, 64, 64) ||
+      !make_tmap(&maps.x_mn, X, H, N, H * 2, 64, 64) ||
+      !make_tmap(&maps.dz_k[0], dz0, p.Vb, p.Nb, p.Vb * 2, kBK, kBM) ||
+      !make_tmap(&maps.dz_k[1], dz1, p.Vb, p.Nb, p.Vb * 2, kBK, kBM) ||
+      !make_tmap(&maps.dz_mn[0], dz0, p.Vb, p.Nb, p.Vb * 2, 64, 64) ||
+      !make_tmap(&maps.dz_mn[1], dz1, p.Vb, p.Nb, p.Vb * 2, 64, 64))
     return FLCE_ERR_CUDA;
 
-  GemmArgs base;
+  // dZ blocks in vocab-major order: b = vb * n_blocks + nb
+  const int nblk = p.n_blocks * p.v_blocks;
+  auto block = [&](int b) {
+    BlockDesc d;
+    const int vb = b / p.n_blocks, nb = b % p.n_blocks;
+    const int64_t row0 = int64_t{nb} * p.Nb, col0 = int64_t{vb} * p.Vb;
+    const int64_t next = std::min<int64_t>(p.Nb, N - row0);
+    const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
+    d.row0 = static_cast<int>(row0);
+    d.col0 = static_cast<int>(col0);
+    d.mt = static_cast<int>(cdiv(next, kBM));
+    d.vt = static_cast<int>(cdiv(vext, kBN));
+    d.vt128 = static_cast<int>(cdiv(vext, kBM));
+    d.slot = b & 1;
+    return d;
+  };
+
+  BwdArgs base;
   std::memset(&base, 0, sizeof(base));
+  base.kb_h = static_cast<int>(cdiv(H, kBK));
   base.N = static_cast<int>(N);
   base.H = static_cast<int>(H);
   base.V = static_cast<int>(V);
   base.targets = targets;
   base.lse = lse;
-  base.dz = dz;
+  base.dz[0] = dz0;
+  base.dz[1] = dz1;
   base.dz_ld = static_cast<int>(p.Vb);
+  if (dX) {
+    if (dx_final)
+      base.dx_final = static_cast<__nv_bfloat16*>(dX);
+    else
+      base.dxf = dxf;
+  }
+  if (dW) {
+    if (dw_final)
+      base.dw_final = static_cast<__nv_bfloat16*>(dW);
+    else
+      base.dwf = dwf;
+  }
   base.grad_loss = grad_loss;
   base.n_valid = nv;
   base.reduction = red;
   base.err = err;
   base.wait_limit_ns = g_wait_limit_ns.load();
-  base.group = 1;
 
-  for (int vb = 0; vb < p.v_blocks; ++vb) {
-    const int64_t col0 = int64_t{vb} * p.Vb;
-    const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
-    const int vt = static_cast<int>(cdiv(vext, kBN));
-    if (dW && !dw_final)
-      FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(vext) * H * 4, s));
-    for (int nb = 0; nb < p.n_blocks; ++nb) {
-      const int64_t row0 = int64_t{nb} * p.Nb;
-      const int64_t next = std::min<int64_t>(p.Nb, N - row0);
-      const int mt = static_cast<int>(cdiv(next, kBM));
-      GemmArgs a = base;
-      a.row0 = static_cast<int>(row0);
-      a.col0 = static_cast<int>(col0);
-      // dZ block = softmax - onehot for rows [row0, row0+next), cols [col0, col0+vext)
-      a.tiles_m = mt;
-      a.tiles_n = vt;
-      a.units = mt * vt;
-      a.k_blocks = static_cast<int>(cdiv(H, kBK));
-      FLCE_CUDA(gemm(kKindR, t_x_k, t_w_k, a, std::min(a.units, dev.sms), s));
-      if (dX) {
-        GemmArgs b = base;
-        b.row0 = a.row0;
-        b.col0 = a.col0;
-        b.tiles_m = mt;
-        b.tiles_n = p.h_tiles;
-        b.units = mt * p.h_tiles;
-        b.k_blocks = vt * (kBN / kBK);
-        if (dx_final)
-          b.final_out = static_cast<__nv_bfloat16*>(dX);
-        else
-          b.acc = dxf;
-        FLCE_CUDA(gemm(kKindX, t_dz_k, t_w_mn, b, std::min(b.units, dev.sms), s));
-      }
-      if (dW) {
-        GemmArgs c = base;
-        c.row0 = a.row0;
-        c.col0 = a.col0;
-        c.tiles_m = static_cast<int>(cdiv(vext, kBM));
-        c.tiles_n = p.h_tiles;
-        c.units = c.tiles_m * p.h_tiles;
-        c.k_blocks = mt * (kBM / kBK);
-        if (dw_final)
-          c.final_out = static_cast<__nv_bfloat16*>(dW);
-        else
-          c.acc = dwf;
-        FLCE_CUDA(gemm(kKindW, t_dz_mn, t_x_mn, c, std::min(c.units, dev.sms), s));
-      }
+  // Launch p: recompute dZ block p (R tiles) while block p-1 is contracted
+  // into dX (X tiles) and dW (W tiles).
+  for (int lp = 0; lp <= nblk; ++lp) {
+    BwdArgs a = base;
+    a.counter = counters + lp;
+    if (lp < nblk) {
+      a.r = block(lp);
+      a.r_tiles = a.r.mt * a.r.vt;
     }
-    if (dW && !dw_final)
+    int xw_vb = -1, xw_nb = -1;
+    if (lp >= 1) {
+      const int b = lp - 1;
+      a.xw = block(b);
+      xw_vb = b / p.n_blocks;
+      xw_nb = b % p.n_blocks;
+      if (dW) a.w_tiles = a.xw.vt128 * p.h_tiles;
+      if (dX) a.x_tiles = a.xw.mt * p.h_tiles;
+      if (dW && !dw_final && xw_nb == 0)
+        FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.xw.vt128) * kBM * H * 4, s));
+    }
+    const int tiles = a.r_tiles + a.w_tiles + a.x_tiles;
+    FLCE_CUDA(profiled(1, s, [&] { return launch_bwd_gemm(maps, a, std::min(tiles, dev.sms), s); }));
+    if (dW && !dw_final && lp >= 1 && xw_nb == p.n_blocks - 1) {
+      const int64_t col0 = int64_t{xw_vb} * p.Vb;
+      const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
       FLCE_CUDA(launch_downcast(dwf, static_cast<__nv_bfloat16*>(dW) + col0 * H,
                                 static_cast<size_t>(vext) * H, grad_loss, nv, red, s));
+    }
   }
   if (dX && !dx_final)
     FLCE_CUDA(launch_downcast(dxf, static_cast<__nv_bfloat16*>(dX), static_cast<size_t>(N) * H,

@@ -36,29 +36,55 @@ enum GemmKind : int {
   kKindW = 3,    // dW tile += dZ_block^T . X_block; A MN-major, B MN-major
 };
 
+// Forward GEMM launch.
 struct GemmArgs {
-  // tile grid of this launch
   int tiles_m, tiles_n, group, units, k_blocks;
-  // coordinate offsets
-  int row0;   // global token row of local row 0 (FWD/R/X: M rows; W: K rows)
-  int col0;   // global vocab index of local column 0 (FWD/R: N cols; X: K rows; W: M rows)
-  // problem sizes
   int N, H, V;
-  // forward
   const int* targets;  // [N], -1 = no valid target
   float2* partials;    // [units_n][N]: per-row (max, sum exp(z - max)) over a work unit
   float* zt;           // [N]: target logit
-  // backward recompute
+  int* err;
+  unsigned long long wait_limit_ns;
+};
+
+// One dZ block of the backward: token rows [row0, row0 + mt*128) x vocab
+// columns [col0, col0 + vt*256), stored in dZ slot `slot`.
+struct BlockDesc {
+  int row0, col0;
+  int mt;     // 128-row token tiles
+  int vt;     // 256-column vocab tiles (R tiles per row tile; X tiles' K / 256)
+  int vt128;  // 128-row vocab tiles of the block's real extent (W tiles' M)
+  int slot;
+};
+
+// Tensor maps of the backward (passed as one __grid_constant__ parameter).
+struct BwdMaps {
+  CUtensorMap x_k;       // X [N][H], box 64 x 128 (R: A operand)
+  CUtensorMap w_k;       // W [V][H], box 64 x 256 (R: B operand)
+  CUtensorMap w_mn;      // W [V][H], box 64 x 64  (X: B operand, MN-major)
+  CUtensorMap x_mn;      // X [N][H], box 64 x 64  (W: B operand, MN-major)
+  CUtensorMap dz_k[2];   // dZ slot [Nb][Vb], box 64 x 128 (X: A operand)
+  CUtensorMap dz_mn[2];  // dZ slot [Nb][Vb], box 64 x 64  (W: A operand, MN-major)
+};
+
+// One backward launch: R tiles of block `r`, W and X tiles of block `xw`.
+struct BwdArgs {
+  BlockDesc r, xw;
+  int r_tiles, w_tiles, x_tiles;
+  int kb_h;  // K blocks of the recompute (ceil(H / 64))
+  int N, H, V;
+  const int* targets;
   const float* lse;
-  __nv_bfloat16* dz;   // dZ block buffer, row-major, dz_ld columns
+  __nv_bfloat16* dz[2];
   int dz_ld;
-  // backward contractions
-  float* acc;                 // FP32 accumulation target (dX: [N][H], dW band: [Vb][H])
-  __nv_bfloat16* final_out;   // if non-null: write bf16(scale * result) here instead
+  float* dxf;                  // FP32 dX accumulator [N][H], or null
+  __nv_bfloat16* dx_final;     // bf16 dX written directly (single vocab block), or null
+  float* dwf;                  // FP32 dW band [Vb][H], or null
+  __nv_bfloat16* dw_final;     // bf16 dW written directly (single token block), or null
   const float* grad_loss;
   const long long* n_valid;
-  int reduction;              // 0 mean, 1 sum
-  // errors / waits
+  int reduction;               // 0 mean, 1 sum
+  int* counter;                // ticket counter of this launch (starts at 0)
   int* err;
   unsigned long long wait_limit_ns;
 };
@@ -71,7 +97,8 @@ struct Plan {
   int64_t Nb, Vb;         // backward block: token rows x vocab columns
   int n_blocks, v_blocks;
   bool multi_n;           // more than one token block: dW needs an FP32 band
-  size_t off_err, off_t, off_zt, off_part, off_lossp, off_nvalid, off_dxf, off_dwf, off_dz;
+  int launches;           // backward GEMM launches (one per dZ block, plus one)
+  size_t off_err, off_t, off_zt, off_part, off_lossp, off_cnt, off_dxf, off_dwf, off_dz;
   size_t total;
 };
 
@@ -94,7 +121,8 @@ cudaError_t launch_downcast(const float* src, __nv_bfloat16* dst, size_t count,
                             const float* grad_loss, const long long* n_valid, int reduction,
                             cudaStream_t st);
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* err, cudaStream_t st);
-cudaError_t launch_gemm(GemmKind kind, const CUtensorMap& ta, const CUtensorMap& tb,
-                        const GemmArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const GemmArgs& a,
+                            int grid, cudaStream_t st);
+cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int grid, cudaStream_t st);
 
 }  // namespace flce

@@ -170,7 +170,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     a.zt = zt;
     a.err = err;
     a.wait_limit_ns = kNoallocWaitNs;
-    if (launch_gemm(kKindFwd, tx, tw, a, std::min(a.units, sms), s) != cudaSuccess)
+    if (launch_fwd_gemm(tx, tw, a, std::min(a.units, sms), s) != cudaSuccess)
       return FLCE_ERR_CUDA;
     int nblocks = 0;
     if (launch_merge_lse(part, static_cast<int>(v_units), static_cast<int>(N), zt, targets, lse,
