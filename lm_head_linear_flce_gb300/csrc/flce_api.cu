@@ -49,17 +49,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer][inner] matrix with 128-byte
-// swizzle; out-of-bounds elements read as zero.
+// 2-D tensor map over a row-major [outer][inner] matrix with 128-byte swizzle;
+// out-of-bounds elements read as zero and are not written.
 bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+  CUresult r = fn(m, dtype, 2, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -164,7 +165,7 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   p->N = N;
   p->H = H;
   p->V = V;
-  p->m_tiles = static_cast<int>(cdiv(N, kBM));
+  p->m_tiles = static_cast<int>(cdiv(N, kPairM));
   p->v_tiles = static_cast<int>(cdiv(V, kBN));
   p->v_units = static_cast<int>(cdiv(p->v_tiles, kFwdGroup));
   p->h_tiles = static_cast<int>(cdiv(H, kBN));
@@ -173,12 +174,12 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   // block when they fit, so dW needs no FP32 accumulator across blocks.
   const int64_t max_rows = g_block_rows.load();
   const int64_t max_elems = g_block_elems.load();
-  const int64_t n_pad = std::max<int64_t>(int64_t{p->m_tiles} * kBM, kBM);
+  const int64_t n_pad = std::max<int64_t>(int64_t{p->m_tiles} * kPairM, kPairM);
   if (n_pad <= max_rows) {
     p->Nb = n_pad;
   } else {
     const int64_t nblk = cdiv(n_pad, max_rows);
-    p->Nb = cdiv(std::max(p->m_tiles, 1), nblk) * kBM;
+    p->Nb = cdiv(std::max(p->m_tiles, 1), nblk) * kPairM;
   }
   const int64_t v_pad = int64_t{p->v_tiles} * kBN;
   p->Vb = std::min<int64_t>(v_pad, std::max<int64_t>(kBN, max_elems / p->Nb / kBN * kBN));
@@ -249,7 +250,7 @@ void flce_set_wait_limit_ns(int64_t limit_ns) {
 }
 
 void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems) {
-  g_block_rows.store(max_rows > 0 ? std::max<int64_t>(max_rows / kBM * kBM, kBM)
+  g_block_rows.store(max_rows > 0 ? std::max<int64_t>(max_rows / kPairM * kPairM, kPairM)
                                   : kDefaultMaxBlockRows);
   g_block_elems.store(max_block_elems > 0 ? max_block_elems : kDefaultDzBlockElems);
 }
@@ -284,7 +285,7 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
                                 reinterpret_cast<long long*>(n_valid), err, s));
 
   CUtensorMap tx, tw;
-  if (!make_tmap(&tx, X, H, N, H * 2, kBK, kBM) || !make_tmap(&tw, W, H, V, H * 2, kBK, kBN))
+  if (!make_tmap(&tx, X, H, N, H * 2, kBK, kBM) || !make_tmap(&tw, W, H, V, H * 2, kBK, kHalfN))
     return FLCE_ERR_CUDA;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -301,7 +302,7 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   a.zt = zt;
   a.err = err;
   a.wait_limit_ns = g_wait_limit_ns.load();
-  FLCE_CUDA(profiled(0, s, [&] { return launch_fwd_gemm(tx, tw, a, std::min(a.units, dev.sms), s); }));
+  FLCE_CUDA(profiled(0, s, [&] { return launch_fwd_gemm(tx, tw, a, a.units, s); }));
   int nblocks = 0;
   FLCE_CUDA(launch_merge_lse(part, p.v_units, static_cast<int>(N), zt, targets, lse, lossp, s,
                              &nblocks));
@@ -352,14 +353,33 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
 
   BwdMaps maps;
   if (!make_tmap(&maps.x_k, X, H, N, H * 2, kBK, kBM) ||
-      !make_tmap(&maps.w_k, W, H, V, H * 2, kBK, kBN) ||
+      !make_tmap(&maps.w_k, W, H, V, H * 2, kBK, kHalfN) ||
       !make_tmap(&maps.w_mn, W, H, V, H * 2, 64, 64) ||
       !make_tmap(&maps.x_mn, X, H, N, H * 2, 64, 64) ||
       !make_tmap(&maps.dz_k[0], dz0, p.Vb, p.Nb, p.Vb * 2, kBK, kBM) ||
       !make_tmap(&maps.dz_k[1], dz1, p.Vb, p.Nb, p.Vb * 2, kBK, kBM) ||
       !make_tmap(&maps.dz_mn[0], dz0, p.Vb, p.Nb, p.Vb * 2, 64, 64) ||
-      !make_tmap(&maps.dz_mn[1], dz1, p.Vb, p.Nb, p.Vb * 2, 64, 64))
+      !make_tmap(&maps.dz_mn[1], dz1, p.Vb, p.Nb, p.Vb * 2, 64, 64) ||
+      !make_tmap(&maps.dz_st[0], dz0, p.Vb, p.Nb, p.Vb * 2, 64, 32) ||
+      !make_tmap(&maps.dz_st[1], dz1, p.Vb, p.Nb, p.Vb * 2, 64, 32))
     return FLCE_ERR_CUDA;
+  // epilogue targets: FP32 accumulators (reduce-add, 32 x 32 boxes) or the bf16
+  // gradients written directly (64 x 32 boxes); an unused map repeats a valid one
+  constexpr CUtensorMapDataType kF32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  bool ok = true;
+  if (dX && dx_final)
+    ok = make_tmap(&maps.dx_out, dX, H, N, H * 2, 64, 32);
+  else if (dX)
+    ok = make_tmap(&maps.dx_out, dxf, H, N, H * 4, 32, 32, kF32);
+  else
+    maps.dx_out = maps.dz_st[0];
+  if (ok && dW && dw_final)
+    ok = make_tmap(&maps.dw_out, dW, H, V, H * 2, 64, 32);
+  else if (ok && dW)
+    ok = make_tmap(&maps.dw_out, dwf, H, p.Vb, H * 4, 32, 32, kF32);
+  else
+    maps.dw_out = maps.dz_st[0];
+  if (!ok) return FLCE_ERR_CUDA;
 
   // dZ blocks in vocab-major order: b = vb * n_blocks + nb
   const int nblk = p.n_blocks * p.v_blocks;
@@ -371,9 +391,8 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
     const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
     d.row0 = static_cast<int>(row0);
     d.col0 = static_cast<int>(col0);
-    d.mt = static_cast<int>(cdiv(next, kBM));
+    d.mt = static_cast<int>(cdiv(next, kPairM));
     d.vt = static_cast<int>(cdiv(vext, kBN));
-    d.vt128 = static_cast<int>(cdiv(vext, kBM));
     d.slot = b & 1;
     return d;
   };
@@ -422,13 +441,13 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
       a.xw = block(b);
       xw_vb = b / p.n_blocks;
       xw_nb = b % p.n_blocks;
-      if (dW) a.w_tiles = a.xw.vt128 * p.h_tiles;
+      if (dW) a.w_tiles = a.xw.vt * p.h_tiles;
       if (dX) a.x_tiles = a.xw.mt * p.h_tiles;
       if (dW && !dw_final && xw_nb == 0)
-        FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.xw.vt128) * kBM * H * 4, s));
+        FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.xw.vt) * kBN * H * 4, s));
     }
     const int tiles = a.r_tiles + a.w_tiles + a.x_tiles;
-    FLCE_CUDA(profiled(1, s, [&] { return launch_bwd_gemm(maps, a, std::min(tiles, dev.sms), s); }));
+    FLCE_CUDA(profiled(1, s, [&] { return launch_bwd_gemm(maps, a, tiles, s); }));
     if (dW && !dw_final && lp >= 1 && xw_nb == p.n_blocks - 1) {
       const int64_t col0 = int64_t{xw_vb} * p.Vb;
       const int64_t vext = std::min<int64_t>(p.Vb, V - col0);

@@ -11,6 +11,12 @@
 //        Mathematical Equivalence), FP32 accumulate.
 //   W    dW += dZ_block^T X_block (dW = dZ^T X, same section), FP32 accumulate.
 //
+// Every tile is 256 x 256 and computed by a pair of CTAs on two SMs (a 2-CTA
+// cluster) with tcgen05 cta_group::2: each CTA stages 128 rows of A and 128 of
+// the 256 columns of B, the even CTA ("leader") issues the MMAs, and each CTA
+// receives its 128 rows of the FP32 result in its own tensor memory.  Per SM
+// this halves the B operand traffic of a 128 x 256 single-CTA tile.
+//
 // Two kernels share the building blocks below:
 //   flce_fwd_kernel  forward; static round-robin over work units of 4 vocab
 //                    tiles of one row tile, so the epilogue can merge the
@@ -19,19 +25,20 @@
 //                    the W and X tiles of block p-1 (two dZ slots, so the
 //                    tiles of one launch never depend on each other).  Tiles
 //                    are handed out by a global atomic ticket, longest first
-//                    (W, then R, then X).
+//                    (W, then R, then X); the leader's producer takes each
+//                    ticket and writes it into both CTAs' ticket rings.
 //
 // CTA layout (192 threads, one CTA per SM, persistent):
-//   warp 0      TMA producer: 4-stage ring of (A 128x64, B 256x64) bf16 tiles,
-//               128-byte swizzled, completion counted on mbarriers.  In the
-//               backward it also takes the tickets and passes them to the other
-//               warps through a small shared-memory ring.
-//   warp 1      allocates 512 TMEM columns; one lane issues tcgen05.mma
-//               (M=128, N=256, K=16) into one of two FP32 accumulators.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w owns TMEM lanes
-//               32*(w%4) .. +31, i.e. tile rows), then the kind's epilogue.
-// The accumulator is double-buffered so the epilogue of tile i overlaps the
-// MMAs of tile i+1.
+//   warp 0      TMA producer: 6-stage ring of (A 128x64, B 128x64) bf16 halves,
+//               128-byte swizzled; both CTAs' copies complete on the leader's
+//               barrier.
+//   warp 1      allocates the 512 TMEM columns of both CTAs; in the leader one
+//               lane issues tcgen05.mma (M=256, N=256, K=16) into one of two
+//               FP32 accumulators and multicasts the commits to both CTAs.
+//   warps 2..5  epilogue: tcgen05.ld of this CTA's accumulator rows (warp w owns
+//               TMEM lanes 32*(w%4) .. +31), then the kind's epilogue.
+#include <algorithm>
+
 #include "flce_device.cuh"
 #include "flce_internal.h"
 
@@ -41,26 +48,33 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTicketRing = 4;
+constexpr uint32_t kStageTx = 2 * (kAStageBytes + kBStageBytes);  // both CTAs of the pair
+constexpr uint16_t kPairMask = 0x3;
 
 struct Smem {
   uint32_t a_base, b_base;  // shared addresses of stage 0 (1024-aligned)
+  uint32_t staging;         // epilogue staging buffers (backward only)
   uint32_t full, empty;     // barrier arrays (stage-indexed, 8 bytes apart)
   uint32_t tfull, tempty;   // accumulator barriers (2 each)
   uint32_t drain;           // MMA drain barrier
   uint32_t qfull, qempty;   // ticket ring barriers
-  volatile int* tickets;    // ticket ring
+  uint32_t tickets;         // ticket ring (shared address)
+  volatile int* tickets_p;  // the same ring, generic pointer
   uint32_t* tmem_slot;
   volatile uint32_t* abort_flag;
 };
 
-// Carves the dynamic shared memory: stages, then barriers, then small slots.
-__device__ Smem carve_smem(uint8_t* smem_raw) {
+// Carves the dynamic shared memory: stages, epilogue staging buffers (if
+// any), then barriers, then small slots.  Identical in both CTAs of a pair, so
+// an offset names the same object in either.
+__device__ Smem carve_smem(uint8_t* smem_raw, uint32_t staging_bytes) {
   Smem s;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   s.a_base = base;
   s.b_base = base + kStages * kAStageBytes;
-  const uint32_t bar0 = s.b_base + kStages * kBStageBytes;
+  s.staging = s.b_base + kStages * kBStageBytes;  // 1024-aligned
+  const uint32_t bar0 = s.staging + staging_bytes;
   s.full = bar0;
   s.empty = s.full + 8 * kStages;
   s.tfull = s.empty + 8 * kStages;
@@ -68,27 +82,28 @@ __device__ Smem carve_smem(uint8_t* smem_raw) {
   s.drain = s.tempty + 8 * kNumAcc;
   s.qfull = s.drain + 8;
   s.qempty = s.qfull + 8 * kTicketRing;
-  const uint32_t tail = s.qempty + 8 * kTicketRing;
-  uint8_t* g = smem_raw + (tail - raw);
-  s.tickets = reinterpret_cast<volatile int*>(g);
-  s.tmem_slot = reinterpret_cast<uint32_t*>(g + 4 * kTicketRing);
-  s.abort_flag = reinterpret_cast<volatile uint32_t*>(g + 4 * kTicketRing + 4);
+  s.tickets = s.qempty + 8 * kTicketRing;
+  s.tickets_p = reinterpret_cast<volatile int*>(smem_raw + (s.tickets - raw));
+  uint8_t* g = smem_raw + (s.tickets + 4 * kTicketRing - raw);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(g);
+  s.abort_flag = reinterpret_cast<volatile uint32_t*>(g + 4);
   return s;
 }
 
 __device__ void init_barriers(const Smem& s) {
   for (int i = 0; i < kStages; ++i) {
-    mbar_init(s.full + 8 * i, 1);
-    mbar_init(s.empty + 8 * i, 1);
+    mbar_init(s.full + 8 * i, 1);   // leader's producer (expect_tx for both CTAs)
+    mbar_init(s.empty + 8 * i, 1);  // the leader's multicast MMA commit
   }
   for (int i = 0; i < kNumAcc; ++i) {
-    mbar_init(s.tfull + 8 * i, 1);
-    mbar_init(s.tempty + 8 * i, 4);
+    mbar_init(s.tfull + 8 * i, 1);   // multicast MMA commit
+    mbar_init(s.tempty + 8 * i, 8);  // 4 epilogue warps in each of the 2 CTAs
   }
   mbar_init(s.drain, 1);
   for (int i = 0; i < kTicketRing; ++i) {
     mbar_init(s.qfull + 8 * i, 1);
-    mbar_init(s.qempty + 8 * i, 1 + 4);  // the MMA lane and the 4 epilogue warps
+    // leader: its MMA lane and 4 epilogue warps; peer: its producer and 4 epilogue warps
+    mbar_init(s.qempty + 8 * i, 10);
   }
   *s.abort_flag = 0u;
   fence_barrier_init();
@@ -119,49 +134,78 @@ __device__ __forceinline__ float grad_scale(const float* grad_loss, const long l
   return n > 0 ? g / static_cast<float>(n) : 0.f;
 }
 
+// Set-up shared by both kernels: barriers, the pair's TMEM, and a cluster
+// barrier so that no CTA signals a barrier of its peer before the peer has
+// initialised it.
+__device__ uint32_t pair_setup(const Smem& s, int warp) {
+  if (threadIdx.x == 0) init_barriers(s);
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(s.tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  return *s.tmem_slot;
+}
+
+// Teardown shared by both kernels: every role has drained; wait for the peer,
+// then release the pair's TMEM.
+__device__ void pair_teardown(uint32_t tmem, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------- k-block operand loads
-// A 128x64 and B 256x64 for Z = X W^T (FWD and R): both K-major.
+// Each CTA loads its own 128 A rows and 128 B columns; completion is counted
+// on the leader's barrier `full` (a shared::cluster address).
+// Z = X W^T (FWD and R): both K-major.
 __device__ __forceinline__ void load_xw(const CUtensorMap* tx, const CUtensorMap* tw, uint32_t sa,
                                         uint32_t sb, int k, int arow, int brow, uint32_t full) {
-  tma_load_2d(sa, tx, k, arow, full);
-  tma_load_2d(sb, tw, k, brow, full);
+  tma_load_2d_pair(sa, tx, k, arow, full);
+  tma_load_2d_pair(sb, tw, k, brow, full);
 }
 // dX tile: A = dZ rows (K-major over vocab), B = W rows of the block (MN-major over H).
 __device__ __forceinline__ void load_dx(const CUtensorMap* tdz, const CUtensorMap* twmn,
-                                        uint32_t sa, uint32_t sb, int k, int m0, int h0,
+                                        uint32_t sa, uint32_t sb, int k, int arow, int h0,
                                         int vrow0, uint32_t full) {
-  tma_load_2d(sa, tdz, k, m0, full);
+  tma_load_2d_pair(sa, tdz, k, arow, full);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * 8192, twmn, h0 + 64 * q, vrow0 + k, full);
+  for (int q = 0; q < 2; ++q) tma_load_2d_pair(sb + q * 8192, twmn, h0 + 64 * q, vrow0 + k, full);
 }
 // dW tile: A = dZ^T (MN-major over vocab), B = X rows of the block (MN-major over H).
 __device__ __forceinline__ void load_dw(const CUtensorMap* tdzmn, const CUtensorMap* txmn,
                                         uint32_t sa, uint32_t sb, int k, int v0, int h0,
                                         int trow0, uint32_t full) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * 8192, tdzmn, v0 + 64 * q, k, full);
+  for (int q = 0; q < 2; ++q) tma_load_2d_pair(sa + q * 8192, tdzmn, v0 + 64 * q, k, full);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * 8192, txmn, h0 + 64 * q, trow0 + k, full);
+  for (int q = 0; q < 2; ++q) tma_load_2d_pair(sb + q * 8192, txmn, h0 + 64 * q, trow0 + k, full);
 }
 
 // ------------------------------------------------------- MMA of one k-block
-// K-major: the 16-element K step is 32 bytes inside the swizzled row.
-// MN-major: it is two 8-row core-matrix groups, 2048 bytes; 64-element groups
-// along M/N are 8192 bytes apart (one 64x64 TMA box each).
+// K-major: the 16-element K step is 32 bytes inside the swizzled row; 8-row
+// groups are 1024 bytes apart.  MN-major: the K step is two 8-row core-matrix
+// groups, 2048 bytes; 64-element groups along M/N are 8192 bytes apart (one
+// 64x64 TMA box each).
 template <bool A_MN, bool B_MN>
 __device__ __forceinline__ void mma_kblock(uint32_t d, uint32_t sa, uint32_t sb, bool first) {
-  constexpr uint32_t idesc = instr_desc_bf16(kBM, kBN, A_MN, B_MN);
+  constexpr uint32_t idesc = instr_desc_bf16(kPairM, kBN, A_MN, B_MN);
 #pragma unroll
   for (int k = 0; k < kBK / kUmmaK; ++k) {
     const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
                              : smem_desc_sw128(sa + k * 32, 0, 1024);
     const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
                              : smem_desc_sw128(sb + k * 32, 0, 1024);
-    mma_bf16(d, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
+    mma_bf16_pair(d, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
   }
 }
 
-// Runs the MMAs of one tile into accumulator d; false if aborted.
+// Leader only: the MMAs of one tile into accumulator d; false if aborted.
 template <bool A_MN, bool B_MN>
 __device__ bool mma_tile(uint32_t d, int k_blocks, const Smem& s, Ring& pipe, const WaitCtx& w) {
   for (int kb = 0; kb < k_blocks; ++kb) {
@@ -169,7 +213,8 @@ __device__ bool mma_tile(uint32_t d, int k_blocks, const Smem& s, Ring& pipe, co
     tc_fence_after();
     mma_kblock<A_MN, B_MN>(d, s.a_base + pipe.idx * kAStageBytes,
                            s.b_base + pipe.idx * kBStageBytes, kb == 0);
-    mma_commit(s.empty + 8 * pipe.idx);  // frees the stage once these MMAs have read it
+    // frees the stage in both CTAs once these MMAs have read it
+    mma_commit_pair_multicast(s.empty + 8 * pipe.idx, kPairMask);
     pipe.advance<kStages>();
   }
   return true;
@@ -210,19 +255,66 @@ __device__ __forceinline__ void epi_lse(uint32_t tbase, int n0, int V, int t, fl
   }
 }
 
-// dZ = exp(Z - lse) - [j == t] (0 for ignored rows and columns >= V), bf16.
-__device__ __forceinline__ void epi_dz(uint32_t tbase, int gcol0, int V, int t, float lse2,
-                                       __nv_bfloat16* out) {
+// ------------------------------------------- staged epilogue (backward)
+// Each epilogue warp owns two 4 KB staging buffers.  A chunk is 32 rows (one
+// per lane) x 128 bytes, written in the 128-byte-swizzled layout of a TMA box
+// (16-byte piece j of row r at (j ^ (r % 8)) * 16), then written to global
+// memory by one TMA store or reduce-add issued by lane 0.  Rows or columns
+// outside the tensor are clipped by the TMA unit.
+struct Stager {
+  uint32_t buf0;
+  uint32_t cur = 0;
+  __device__ uint32_t buf() const { return buf0 + cur * kStageBufBytes; }
+  // the buffer about to be filled was last used two chunks ago
+  __device__ void acquire(int lane) {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+  }
+  __device__ void write_row(int lane, const uint32_t (&w)[32]) const {
+    const uint32_t row = buf() + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(row + ((j ^ (lane & 7)) << 4),
+                   make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]));
+  }
+  // make the generic-proxy writes visible to the TMA unit, then hand over
+  __device__ void publish() {
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+  __device__ void store(int lane, const CUtensorMap* m, int x, int y) {
+    publish();
+    if (lane == 0) {
+      tma_store_2d(m, buf(), x, y);
+      bulk_commit();
+    }
+    cur ^= 1u;
+  }
+  __device__ void reduce_add(int lane, const CUtensorMap* m, int x, int y) {
+    publish();
+    if (lane == 0) {
+      tma_reduce_add_2d(m, buf(), x, y);
+      bulk_commit();
+    }
+    cur ^= 1u;
+  }
+};
+
+// dZ tile rows of this warp: 64 columns per chunk, bf16 store into the slot.
+__device__ __forceinline__ void epi_dz_staged(uint32_t tbase, int gcol0, int V, int t, float lse2,
+                                              Stager& st, int lane, const CUtensorMap* m, int x0,
+                                              int y) {
   const bool valid_row = t >= 0;
 #pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
-    float v[32];
-    tmem_ld32(tbase + 32 * c, v);
-    const int j0 = gcol0 + 32 * c;
-    uint32_t p[16];
+  for (int c = 0; c < kBN / 64; ++c) {
+    float v[64];
+    tmem_ld32(tbase + 64 * c, *reinterpret_cast<float(*)[32]>(&v[0]));
+    tmem_ld32(tbase + 64 * c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+    const int j0 = gcol0 + 64 * c;
+    uint32_t p[32];
     if (valid_row) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
+      for (int i = 0; i < 64; i += 2) {
         float d0 = exp2f(fmaf(v[i], kLog2e, -lse2));
         float d1 = exp2f(fmaf(v[i + 1], kLog2e, -lse2));
         if (j0 + i == t) d0 -= 1.f;
@@ -233,52 +325,54 @@ __device__ __forceinline__ void epi_dz(uint32_t tbase, int gcol0, int V, int t, 
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) p[i] = 0u;
+      for (int i = 0; i < 32; ++i) p[i] = 0u;
     }
-    uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+    st.acquire(lane);
+    st.write_row(lane, p);
+    st.store(lane, m, x0 + 64 * c, y);
   }
 }
 
-// FP32 reduce-add of one accumulator row into acc_row[h0 ...], or, when
-// final_row is set, bf16(scale * value) stored there.
-__device__ __forceinline__ void epi_acc(uint32_t tbase, int h0, int H, bool row_ok,
-                                        float* acc_row, __nv_bfloat16* final_row, float scale) {
+// FP32 accumulator rows: reduce-add 32 columns per chunk into the FP32 buffer.
+__device__ __forceinline__ void epi_reduce_staged(uint32_t tbase, int h0, int H, Stager& st,
+                                                  int lane, const CUtensorMap* m, int y) {
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     const int h = h0 + 32 * c;
     if (h >= H) break;  // warp-uniform
     float v[32];
     tmem_ld32(tbase + 32 * c, v);
-    if (!row_ok) continue;
-    if (final_row) {
-      __nv_bfloat16* o = final_row + h;
+    uint32_t w[32];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (h + 8 * i < H) {
-          uint4 pk = make_uint4(pack_bf16x2(scale * v[8 * i], scale * v[8 * i + 1]),
-                                pack_bf16x2(scale * v[8 * i + 2], scale * v[8 * i + 3]),
-                                pack_bf16x2(scale * v[8 * i + 4], scale * v[8 * i + 5]),
-                                pack_bf16x2(scale * v[8 * i + 6], scale * v[8 * i + 7]));
-          *reinterpret_cast<uint4*>(o + 8 * i) = pk;
-        }
-      }
-    } else {
-      float* o = acc_row + h;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (h + 4 * i < H)
-          atomicAdd(reinterpret_cast<float4*>(o + 4 * i),
-                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
-      }
-    }
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+    st.acquire(lane);
+    st.write_row(lane, w);
+    st.reduce_add(lane, m, h, y);
   }
 }
 
-// Producer teardown: every stage's most recent load must have landed before
-// the CTA may exit (its shared memory is the copy's destination).
+// Final gradient rows: bf16(scale * acc), 64 columns per chunk.
+__device__ __forceinline__ void epi_final_staged(uint32_t tbase, int h0, int H, float scale,
+                                                 Stager& st, int lane, const CUtensorMap* m,
+                                                 int y) {
+#pragma unroll 1
+  for (int c = 0; c < kBN / 64; ++c) {
+    const int h = h0 + 64 * c;
+    if (h >= H) break;  // warp-uniform
+    float v[64];
+    tmem_ld32(tbase + 64 * c, *reinterpret_cast<float(*)[32]>(&v[0]));
+    tmem_ld32(tbase + 64 * c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+    uint32_t p[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) p[i] = pack_bf16x2(scale * v[2 * i], scale * v[2 * i + 1]);
+    st.acquire(lane);
+    st.write_row(lane, p);
+    st.store(lane, m, h, y);
+  }
+}
+
+// Leader's producer teardown: every stage's most recent loads (from both CTAs)
+// must have landed before either CTA may exit.
 __device__ void drain_loads(const Smem& s, uint32_t issued, const Ring& pipe, const WaitCtx& w0) {
   WaitCtx wd = w0;
   volatile uint32_t never = 0u;
@@ -291,8 +385,9 @@ __device__ void drain_loads(const Smem& s, uint32_t issued, const Ring& pipe, co
   }
 }
 
+// Leader's MMA teardown: all issued MMAs complete before TMEM is released.
 __device__ void drain_mma(const Smem& s, const WaitCtx& w0) {
-  mma_commit(s.drain);
+  mma_commit_pair(s.drain);
   WaitCtx wd = w0;
   volatile uint32_t never = 0u;
   wd.abort = &never;
@@ -300,13 +395,13 @@ __device__ void drain_mma(const Smem& s, const WaitCtx& w0) {
 }
 
 // ======================================================================= FWD
-// Units are dealt round robin; a unit is `group` consecutive vocab tiles of one
-// row tile.  Units with the same vocab group are adjacent so CTAs running at
-// the same time share the W rows in L2.
+// Units are dealt round robin over the CTA pairs; a unit is `group`
+// consecutive vocab tiles of one row tile.  Units with the same vocab group are
+// adjacent so pairs running at the same time share the W rows in L2.
 struct FwdSeq {
   int unit, g;
   __device__ void begin() {
-    unit = blockIdx.x;
+    unit = blockIdx.x >> 1;
     g = 0;
   }
   __device__ bool valid(const GemmArgs& a) const { return unit < a.units; }
@@ -317,7 +412,7 @@ struct FwdSeq {
   }
   __device__ void next(const GemmArgs& a) {
     if (last_in_unit(a)) {
-      unit += gridDim.x;
+      unit += gridDim.x >> 1;
       g = 0;
     } else {
       ++g;
@@ -327,26 +422,20 @@ struct FwdSeq {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     flce_fwd_kernel(const __grid_constant__ CUtensorMap tma_x,
                     const __grid_constant__ CUtensorMap tma_w, const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const Smem s = carve_smem(smem_raw);
+  const Smem s = carve_smem(smem_raw, 0);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
   if (threadIdx.x == 0) {
-    init_barriers(s);
     tma_prefetch_desc(&tma_x);
     tma_prefetch_desc(&tma_w);
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(s.tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s.tmem_slot;
+  const uint32_t tmem = pair_setup(s, warp);
   const WaitCtx w{s.abort_flag, a.err, a.wait_limit_ns};
 
   if (warp == 0) {
@@ -355,43 +444,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t issued = 0;
       FwdSeq seq;
       for (seq.begin(); seq.valid(a); seq.next(a)) {
-        const int m0 = seq.mt(a) * kBM, n0 = seq.nt(a) * kBN;
+        const int arow = seq.mt(a) * kPairM + kBM * rank;
+        const int brow = seq.nt(a) * kBN + kHalfN * rank;
         bool ok = true;
         for (int kb = 0; kb < a.k_blocks && ok; ++kb) {
           ok = wait_parity(s.empty + 8 * pipe.idx, pipe.phase ^ 1u, w);
           if (!ok) break;
           const uint32_t full = s.full + 8 * pipe.idx;
-          mbar_arrive_expect_tx(full, kAStageBytes + kBStageBytes);
+          if (leader) mbar_arrive_expect_tx(full, kStageTx);
           load_xw(&tma_x, &tma_w, s.a_base + pipe.idx * kAStageBytes,
-                  s.b_base + pipe.idx * kBStageBytes, kb * kBK, m0, n0, full);
+                  s.b_base + pipe.idx * kBStageBytes, kb * kBK, arow, brow,
+                  mapa_shared(full, 0));
           issued |= 1u << pipe.idx;
           pipe.advance<kStages>();
         }
         if (!ok) break;
       }
-      drain_loads(s, issued, pipe, w);
+      if (leader) drain_loads(s, issued, pipe, w);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       Ring pipe, accr;
       FwdSeq seq;
       for (seq.begin(); seq.valid(a); seq.next(a)) {
-        if (!wait_parity(s.tempty + 8 * accr.idx, accr.phase ^ 1u, w)) break;
+        if (!wait_parity_cluster(s.tempty + 8 * accr.idx, accr.phase ^ 1u, w)) break;
         tc_fence_after();
         if (!mma_tile<false, false>(tmem + accr.idx * kAccCols, a.k_blocks, s, pipe, w)) break;
-        mma_commit(s.tfull + 8 * accr.idx);
+        mma_commit_pair_multicast(s.tfull + 8 * accr.idx, kPairMask);
         accr.advance<kNumAcc>();
       }
       drain_mma(s, w);
     }
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;
+    const int r = kBM * rank + q * 32 + lane;  // row of the 256-row tile
     Ring accr;
     float run_m = -INFINITY, run_s = 0.f;
     FwdSeq seq;
     for (seq.begin(); seq.valid(a); seq.next(a)) {
-      const int row = seq.mt(a) * kBM + r;
+      const int row = seq.mt(a) * kPairM + r;
       const int n0 = seq.nt(a) * kBN;
       const int t = row < a.N ? a.targets[row] : -1;
       if (seq.g == 0) {
@@ -405,7 +496,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       epi_lse(tbase, n0, a.V, t, a.zt + (row < a.N ? row : 0), run_m, run_s);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s.tempty + 8 * accr.idx);
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(s.tempty + 8 * accr.idx, 0));
       accr.advance<kNumAcc>();
       if (seq.last_in_unit(a) && row < a.N) {
         const int chunk = seq.nt(a) / a.group;
@@ -413,11 +504,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  pair_teardown(tmem, warp);
 }
 
 // ======================================================================= BWD
@@ -432,37 +519,31 @@ struct Tile {
 // share the operand that is reused most (the H columns or the vocab rows).
 __device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, int t) {
   if (t < a.w_tiles) {
-    const int v = t % a.xw.vt128, h = t / a.xw.vt128;
-    return {kKindW, v * kBM, h * kBN, a.xw.mt * (kBM / kBK)};
+    const int v = t % a.xw.vt, h = t / a.xw.vt;
+    return {kKindW, v * kPairM, h * kBN, a.xw.mt * (kPairM / kBK)};
   }
   t -= a.w_tiles;
   if (t < a.r_tiles) {
     const int m = t % a.r.mt, v = t / a.r.mt;
-    return {kKindR, m * kBM, v * kBN, a.kb_h};
+    return {kKindR, m * kPairM, v * kBN, a.kb_h};
   }
   t -= a.r_tiles;
   const int m = t % a.xw.mt, h = t / a.xw.mt;
-  return {kKindX, m * kBM, h * kBN, a.xw.vt * (kBN / kBK)};
+  return {kKindX, m * kPairM, h * kBN, a.xw.vt * (kBN / kBK)};
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     flce_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const Smem s = carve_smem(smem_raw);
+  const Smem s = carve_smem(smem_raw, 4 * 2 * kStageBufBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
   const int total = a.w_tiles + a.r_tiles + a.x_tiles;
-  if (threadIdx.x == 0) init_barriers(s);
-  if (warp == 1) {
-    tmem_alloc(smem_u32(s.tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s.tmem_slot;
+  const uint32_t tmem = pair_setup(s, warp);
   const WaitCtx w{s.abort_flag, a.err, a.wait_limit_ns};
 
   if (warp == 0) {
@@ -472,46 +553,60 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const CUtensorMap* dz_k = &maps.dz_k[a.xw.slot & 1];
       const CUtensorMap* dz_mn = &maps.dz_mn[a.xw.slot & 1];
       for (;;) {
-        const int t = atomicAdd(a.counter, 1);
-        if (!wait_parity(s.qempty + 8 * ring.idx, ring.phase ^ 1u, w)) break;
-        s.tickets[ring.idx] = t;
-        mbar_arrive(s.qfull + 8 * ring.idx);
+        int t;
+        if (leader) {
+          // take a ticket and publish it in both CTAs' rings
+          t = atomicAdd(a.counter, 1);
+          if (!wait_parity_cluster(s.qempty + 8 * ring.idx, ring.phase ^ 1u, w)) break;
+          s.tickets_p[ring.idx] = t;
+          st_shared_cluster_u32(mapa_shared(s.tickets + 4 * ring.idx, 1),
+                                static_cast<uint32_t>(t));
+          mbar_arrive(s.qfull + 8 * ring.idx);
+          mbar_arrive_cluster(mapa_shared(s.qfull + 8 * ring.idx, 1));
+        } else {
+          if (!wait_parity_cluster(s.qfull + 8 * ring.idx, ring.phase, w)) break;
+          t = s.tickets_p[ring.idx];
+          mbar_arrive_cluster(mapa_shared(s.qempty + 8 * ring.idx, 0));
+        }
         ring.advance<kTicketRing>();
         if (t >= total) break;
         const Tile tile = decode_ticket(a, t);
+        const int arow = tile.m0 + kBM * rank;     // this CTA's A rows (M)
+        const int bcol = tile.n0 + kHalfN * rank;  // this CTA's B columns (N)
         bool ok = true;
         for (int kb = 0; kb < tile.k_blocks; ++kb) {
           ok = wait_parity(s.empty + 8 * pipe.idx, pipe.phase ^ 1u, w);
           if (!ok) break;
           const uint32_t full = s.full + 8 * pipe.idx;
+          const uint32_t full_c = mapa_shared(full, 0);
           const uint32_t sa = s.a_base + pipe.idx * kAStageBytes;
           const uint32_t sb = s.b_base + pipe.idx * kBStageBytes;
           const int k = kb * kBK;
-          mbar_arrive_expect_tx(full, kAStageBytes + kBStageBytes);
+          if (leader) mbar_arrive_expect_tx(full, kStageTx);
           if (tile.kind == kKindR)
-            load_xw(&maps.x_k, &maps.w_k, sa, sb, k, a.r.row0 + tile.m0, a.r.col0 + tile.n0, full);
+            load_xw(&maps.x_k, &maps.w_k, sa, sb, k, a.r.row0 + arow, a.r.col0 + bcol, full_c);
           else if (tile.kind == kKindX)
-            load_dx(dz_k, &maps.w_mn, sa, sb, k, tile.m0, tile.n0, a.xw.col0, full);
+            load_dx(dz_k, &maps.w_mn, sa, sb, k, arow, bcol, a.xw.col0, full_c);
           else
-            load_dw(dz_mn, &maps.x_mn, sa, sb, k, tile.m0, tile.n0, a.xw.row0, full);
+            load_dw(dz_mn, &maps.x_mn, sa, sb, k, arow, bcol, a.xw.row0, full_c);
           issued |= 1u << pipe.idx;
           pipe.advance<kStages>();
         }
         if (!ok) break;
       }
-      drain_loads(s, issued, pipe, w);
+      if (leader) drain_loads(s, issued, pipe, w);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       Ring pipe, accr, ring;
       for (;;) {
         if (!wait_parity(s.qfull + 8 * ring.idx, ring.phase, w)) break;
-        const int t = s.tickets[ring.idx];
+        const int t = s.tickets_p[ring.idx];
         mbar_arrive(s.qempty + 8 * ring.idx);
         ring.advance<kTicketRing>();
         if (t >= total) break;
         const Tile tile = decode_ticket(a, t);
-        if (!wait_parity(s.tempty + 8 * accr.idx, accr.phase ^ 1u, w)) break;
+        if (!wait_parity_cluster(s.tempty + 8 * accr.idx, accr.phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem + accr.idx * kAccCols;
         bool ok;
@@ -522,31 +617,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else
           ok = mma_tile<true, true>(d, tile.k_blocks, s, pipe, w);
         if (!ok) break;
-        mma_commit(s.tfull + 8 * accr.idx);
+        mma_commit_pair_multicast(s.tfull + 8 * accr.idx, kPairMask);
         accr.advance<kNumAcc>();
       }
       drain_mma(s, w);
     }
   } else {
     const int q = warp & 3;
-    const int r = q * 32 + lane;
+    const int r = kBM * rank + q * 32 + lane;  // row of the 256-row tile
     // scale g / n_valid (mean) or g (sum), applied when a tile writes bf16 directly
     const float scale =
         (a.dx_final || a.dw_final) ? grad_scale(a.grad_loss, a.n_valid, a.reduction) : 1.f;
+    Stager st;
+    st.buf0 = s.staging + static_cast<uint32_t>(q) * 2 * kStageBufBytes;
     Ring accr, ring;
     for (;;) {
-      if (!wait_parity(s.qfull + 8 * ring.idx, ring.phase, w)) break;
-      const int t = s.tickets[ring.idx];
+      if (!wait_parity_cluster(s.qfull + 8 * ring.idx, ring.phase, w)) break;
+      const int t = s.tickets_p[ring.idx];
       __syncwarp();
-      if (lane == 0) mbar_arrive(s.qempty + 8 * ring.idx);
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(s.qempty + 8 * ring.idx, 0));
       ring.advance<kTicketRing>();
       if (t >= total) break;
       const Tile tile = decode_ticket(a, t);
       // per-row context, read before waiting for the accumulator
-      int grow = 0, tgt = -1;
+      int tgt = -1;
       float lse2 = 0.f;
       if (tile.kind == kKindR) {
-        grow = a.r.row0 + tile.m0 + r;
+        const int grow = a.r.row0 + tile.m0 + r;
         if (grow < a.N) {
           tgt = a.targets[grow];
           lse2 = a.lse[grow] * kLog2e;
@@ -556,42 +653,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(q * 32) << 16) + accr.idx * kAccCols;
+      const int y0 = tile.m0 + r - lane;  // first tile row of this warp
       if (tile.kind == kKindR) {
-        __nv_bfloat16* out = a.dz[a.r.slot & 1] +
-                             static_cast<size_t>(tile.m0 + r) * a.dz_ld + tile.n0;
-        epi_dz(tbase, a.r.col0 + tile.n0, a.V, tgt, lse2, out);
+        epi_dz_staged(tbase, a.r.col0 + tile.n0, a.V, tgt, lse2, st, lane,
+                      &maps.dz_st[a.r.slot & 1], tile.n0, y0);
       } else if (tile.kind == kKindX) {
-        const int row = a.xw.row0 + tile.m0 + r;
-        const bool ok = row < a.N;
-        epi_acc(tbase, tile.n0, a.H, ok,
-                a.dxf ? a.dxf + static_cast<size_t>(row) * a.H : nullptr,
-                a.dx_final ? a.dx_final + static_cast<size_t>(row) * a.H : nullptr, scale);
+        if (a.dx_final)
+          epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dx_out, a.xw.row0 + y0);
+        else
+          epi_reduce_staged(tbase, tile.n0, a.H, st, lane, &maps.dx_out, a.xw.row0 + y0);
       } else {
-        const int lv = tile.m0 + r;
-        const int v = a.xw.col0 + lv;
-        const bool ok = v < a.V;
-        epi_acc(tbase, tile.n0, a.H, ok,
-                a.dwf ? a.dwf + static_cast<size_t>(lv) * a.H : nullptr,
-                a.dw_final ? a.dw_final + static_cast<size_t>(v) * a.H : nullptr, scale);
+        if (a.dw_final)
+          epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dw_out, a.xw.col0 + y0);
+        else
+          epi_reduce_staged(tbase, tile.n0, a.H, st, lane, &maps.dw_out, y0);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s.tempty + 8 * accr.idx);
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(s.tempty + 8 * accr.idx, 0));
       accr.advance<kNumAcc>();
     }
+    // all staged stores and reductions complete before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  pair_teardown(tmem, warp);
 }
 
 // ================================================================= launchers
+namespace {
+
+// CTA pairs of `kernel` that fit on the device at once (cached per kernel).
+int max_pairs(const void* kernel, int smem, int* cache) {
+  if (*cache > 0) return *cache;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  *cache = n;
+  return n;
+}
+
+}  // namespace
+
 cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const GemmArgs& a,
-                            int grid, cudaStream_t st) {
-  if (grid <= 0) return cudaSuccess;
+                            int units, cudaStream_t st) {
+  if (units <= 0) return cudaSuccess;
   static bool attr = false;
+  static int pairs = 0;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(flce_fwd_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -599,22 +723,27 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  flce_fwd_kernel<<<grid, kGemmThreads, kGemmSmemBytes, st>>>(tx, tw, a);
+  const int n = std::min(units, max_pairs(reinterpret_cast<const void*>(flce_fwd_kernel),
+                                          kGemmSmemBytes, &pairs));
+  flce_fwd_kernel<<<2 * n, kGemmThreads, kGemmSmemBytes, st>>>(tx, tw, a);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int grid, cudaStream_t st) {
-  if (grid <= 0) return cudaSuccess;
+cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, cudaStream_t st) {
+  if (units <= 0) return cudaSuccess;
   static bool attr = false;
+  static int pairs = 0;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(flce_bwd_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGemmSmemBytes);
+                                         kBwdSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  flce_bwd_kernel<<<grid, kGemmThreads, kGemmSmemBytes, st>>>(maps, a);
+  const int n = std::min(units, max_pairs(reinterpret_cast<const void*>(flce_bwd_kernel),
+                                          kBwdSmemBytes, &pairs));
+  flce_bwd_kernel<<<2 * n, kGemmThreads, kBwdSmemBytes, st>>>(maps, a);
   note_launch();
   return cudaGetLastError();
 }

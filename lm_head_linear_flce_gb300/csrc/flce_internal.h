@@ -13,20 +13,29 @@ namespace flce {
 constexpr int kErrLabel = 1;    // a target outside [0, V) that is not ignore_index
 constexpr int kErrTimeout = 2;  // a bounded wait ran out
 
-// GEMM tile geometry (all tensor-core kernels).
-constexpr int kBM = 128;        // rows of a tile (MMA M)
-constexpr int kBN = 256;        // columns of a tile (MMA N)
+// GEMM tile geometry (all tensor-core kernels).  Tiles are computed by a pair
+// of CTAs (a 2-CTA cluster on two SMs) with tcgen05 cta_group::2: a tile is
+// 256 rows x 256 columns; each CTA holds 128 rows of A and 128 of the 256 B
+// columns in shared memory and 128 rows x 256 columns of the FP32 result in
+// its tensor memory.
+constexpr int kPairM = 256;     // tile rows over the pair (MMA M)
+constexpr int kBM = 128;        // tile rows per CTA
+constexpr int kBN = 256;        // tile columns (MMA N)
+constexpr int kHalfN = 128;     // B columns per CTA
 constexpr int kBK = 64;         // K per pipeline stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;      // K per tcgen05.mma (bf16)
-constexpr int kStages = 4;      // shared-memory pipeline depth
-constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
-constexpr int kBStageBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kStages = 6;      // shared-memory pipeline depth
+constexpr int kAStageBytes = kBM * kBK * 2;     // 16 KB
+constexpr int kBStageBytes = kHalfN * kBK * 2;  // 16 KB
 constexpr int kAccCols = kBN;   // FP32 accumulator columns per tile
 constexpr int kNumAcc = 2;      // double-buffered accumulators
 constexpr int kTmemCols = kAccCols * kNumAcc;  // 512: the whole tensor memory
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kFwdGroup = 4;    // vocab tiles merged per forward work unit
 constexpr int kGemmSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*align*/ + 256;
+// backward epilogue staging: per epilogue warp two 4 KB buffers (32 rows x 128 B)
+constexpr int kStageBufBytes = 4096;
+constexpr int kBwdSmemBytes = kGemmSmemBytes + 4 * 2 * kStageBufBytes;
 
 // Kinds of GEMM tile.
 enum GemmKind : int {
@@ -47,24 +56,29 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;
 };
 
-// One dZ block of the backward: token rows [row0, row0 + mt*128) x vocab
+// One dZ block of the backward: token rows [row0, row0 + mt*256) x vocab
 // columns [col0, col0 + vt*256), stored in dZ slot `slot`.
 struct BlockDesc {
   int row0, col0;
-  int mt;     // 128-row token tiles
-  int vt;     // 256-column vocab tiles (R tiles per row tile; X tiles' K / 256)
-  int vt128;  // 128-row vocab tiles of the block's real extent (W tiles' M)
+  int mt;     // 256-row token tiles
+  int vt;     // 256-column vocab tiles (R tiles per row tile; W tiles; X tiles' K / 256)
   int slot;
 };
 
 // Tensor maps of the backward (passed as one __grid_constant__ parameter).
 struct BwdMaps {
   CUtensorMap x_k;       // X [N][H], box 64 x 128 (R: A operand)
-  CUtensorMap w_k;       // W [V][H], box 64 x 256 (R: B operand)
+  CUtensorMap w_k;       // W [V][H], box 64 x 128 (R: B operand, one CTA's half)
   CUtensorMap w_mn;      // W [V][H], box 64 x 64  (X: B operand, MN-major)
   CUtensorMap x_mn;      // X [N][H], box 64 x 64  (W: B operand, MN-major)
   CUtensorMap dz_k[2];   // dZ slot [Nb][Vb], box 64 x 128 (X: A operand)
   CUtensorMap dz_mn[2];  // dZ slot [Nb][Vb], box 64 x 64  (W: A operand, MN-major)
+  // epilogue stores, box = one warp's 32 rows x 128 bytes
+  CUtensorMap dz_st[2];  // dZ slot [Nb][Vb] bf16, box 64 x 32 (R: dZ store)
+  CUtensorMap dx_out;    // dX accumulator [N][H] f32 box 32 x 32 (reduce-add), or
+                         // dX [N][H] bf16 box 64 x 32 (store) when written directly
+  CUtensorMap dw_out;    // dW band [Vb][H] f32 box 32 x 32 (reduce-add), or
+                         // dW [V][H] bf16 box 64 x 32 (store) when written directly
 };
 
 // One backward launch: R tiles of block `r`, W and X tiles of block `xw`.
@@ -121,8 +135,10 @@ cudaError_t launch_downcast(const float* src, __nv_bfloat16* dst, size_t count,
                             const float* grad_loss, const long long* n_valid, int reduction,
                             cudaStream_t st);
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* err, cudaStream_t st);
+// Tensor-core launches: `units` work items over at most as many CTA pairs as
+// fit on the device at once.
 cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const GemmArgs& a,
-                            int grid, cudaStream_t st);
-cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int grid, cudaStream_t st);
+                            int units, cudaStream_t st);
+cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, cudaStream_t st);
 
 }  // namespace flce

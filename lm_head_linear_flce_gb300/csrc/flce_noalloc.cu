@@ -118,7 +118,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     if (N % S != 0) return FLCE_ERR_INVALID_ARG;
   }
   // scratch layout: error word | targets | target logits | lse partials | loss partials
-  const int64_t m_tiles = (N + kBM - 1) / kBM;
+  const int64_t m_tiles = (N + kPairM - 1) / kPairM;
   const int64_t v_tiles = (V + kBN - 1) / kBN;
   const int64_t v_units = (v_tiles + kFwdGroup - 1) / kFwdGroup;
   const size_t off_t = up(16);
@@ -153,7 +153,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
                             err, s) != cudaSuccess)
       return FLCE_ERR_CUDA;
     CUtensorMap tx, tw;
-    if (!encode_bf16_map(&tx, X, H, N, kBK, kBM) || !encode_bf16_map(&tw, W, H, V, kBK, kBN))
+    if (!encode_bf16_map(&tx, X, H, N, kBK, kBM) || !encode_bf16_map(&tw, W, H, V, kBK, kHalfN))
       return FLCE_ERR_CUDA;
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -170,7 +170,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     a.zt = zt;
     a.err = err;
     a.wait_limit_ns = kNoallocWaitNs;
-    if (launch_fwd_gemm(tx, tw, a, std::min(a.units, sms), s) != cudaSuccess)
+    if (launch_fwd_gemm(tx, tw, a, a.units, s) != cudaSuccess)
       return FLCE_ERR_CUDA;
     int nblocks = 0;
     if (launch_merge_lse(part, static_cast<int>(v_units), static_cast<int>(N), zt, targets, lse,
