@@ -352,7 +352,7 @@ def main(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-rows", type=int, default=384)
+    p.add_argument("--cpu-rows", type=int, default=1024)
     p.add_argument("--ref-rows", type=int, default=8)
     p.add_argument("--tokens", type=int, default=0, help="override N (profiling cases)")
     p.add_argument("--vocab", type=int, default=0, help="override V (profiling cases)")

@@ -137,8 +137,8 @@ void flce_set_wait_limit_ns(int64_t limit_ns);
 
 /*
  * Tuning: caps the backward's dZ block at `max_rows` token rows (rounded down
- * to a multiple of 128, at least 128) and `max_block_elems` bf16 elements
- * (default 8192 rows and 16 Mi elements, a 32 MB block that stays in L2).
+ * to a multiple of 256, at least 256) and `max_block_elems` bf16 elements
+ * (default 8192 rows and 32 Mi elements, a 64 MB block).
  * Smaller blocks mean less workspace and more FP32 accumulation traffic.
  * Values <= 0 restore the defaults.  Process-wide; flce_workspace_size and the
  * calls that use the workspace must see the same setting.
@@ -151,9 +151,11 @@ void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems);
  * flce_kernel_launch_count: kernels this library has launched in this process
  * (tensor-core GEMMs and the small SIMT kernels; memsets not included).
  *
- * flce_profile_enable(1) makes every later tensor-core kernel launch record a
- * CUDA event on the launching stream just before and just after it (events
- * come from a pool the library owns; no device memory is allocated).
+ * flce_profile_enable(1) makes later calls record CUDA events on the call's
+ * stream around their tensor-core launches (events come from a pool the
+ * library owns; no device memory is allocated): around the forward GEMM
+ * launch, and around the whole run of backward GEMM launches of a call (those
+ * launches overlap one another, so they are timed as one interval).
  * flce_profile_collect waits for those events, writes per-kind totals into
  * ms[4] and launches[4] (index 0: forward GEMM with its log-sum-exp epilogue,
  * 1: backward GEMM launches, each holding dZ-recompute, dX and dW tiles;

@@ -19,7 +19,7 @@ namespace {
 
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;
 constexpr int64_t kMaxH = 1 << 16;
-constexpr int64_t kDefaultDzBlockElems = int64_t{16} << 20;  // bf16 dZ block: 32 MB, L2-resident
+constexpr int64_t kDefaultDzBlockElems = int64_t{32} << 20;  // bf16 dZ block: 64 MB
 constexpr int64_t kDefaultMaxBlockRows = 8192;
 constexpr size_t kAlign = 256;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
@@ -61,6 +61,23 @@ bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dtype, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D view (64 elements, rows, 64-element groups) of a row-major matrix with
+// `inner` (a multiple of 64) elements per row: box 64 x 64 rows x 2 groups is
+// one 128-column MN-major operand half in the 128-byte-swizzled layout.
+bool make_tmap_mn3(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
+                   uint64_t row_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || inner % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, inner / 64};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, 64, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -122,6 +139,7 @@ std::mutex g_prof_mu;
 struct ProfRec {
   int kind;
   cudaEvent_t a, b;
+  int launches = 1;
 };
 std::vector<ProfRec> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
@@ -142,12 +160,33 @@ template <class F>
 cudaError_t profiled(int kind, cudaStream_t s, F&& launch) {
   if (!g_prof_on.load()) return launch();
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  ProfRec r{kind, take_event(), take_event()};
+  ProfRec r{kind, take_event(), take_event(), 1};
   if (r.a) cudaEventRecord(r.a, s);
   cudaError_t e = launch();
   if (r.b) cudaEventRecord(r.b, s);
   if (r.a && r.b) g_prof.push_back(r);
   return e;
+}
+
+// Brackets a run of consecutive launches (which may overlap each other) with
+// one pair of profiling events; `launches` is how many the run holds.
+ProfRec g_open{-1, nullptr, nullptr, 0};
+void prof_begin(cudaStream_t s) {
+  if (!g_prof_on.load()) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_open.a = take_event();
+  if (g_open.a) cudaEventRecord(g_open.a, s);
+}
+void prof_end(int kind, int launches, cudaStream_t s) {
+  if (!g_prof_on.load()) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_open.a) return;
+  ProfRec r{kind, g_open.a, take_event(), launches};
+  g_open.a = nullptr;
+  if (!r.b) return;
+  cudaEventRecord(r.b, s);
+  r.launches = launches;
+  g_prof.push_back(r);
 }
 
 #define FLCE_CUDA(x)                         \
@@ -210,8 +249,11 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   if (p->v_blocks > 1) off = align_up(off + static_cast<size_t>(N) * H * 4);
   p->off_dwf = off;
   if (p->multi_n) off = align_up(off + static_cast<size_t>(p->Vb) * H * 4);
-  p->off_dz = off;  // two slots: block p is formed while block p-1 is consumed
-  off = align_up(off + 2 * static_cast<size_t>(p->Nb) * p->Vb * 2);
+  // two slots: block p is formed while block p-1 is consumed.  Rows are padded
+  // by 64 elements so that the row pitch is not a power of two.
+  p->dz_ld = p->Vb + 64;
+  p->off_dz = off;
+  off = align_up(off + 2 * static_cast<size_t>(p->Nb) * p->dz_ld * 2);
   p->total = std::max(fwd_end, off);
   return true;
 }
@@ -345,7 +387,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
   float* dwf = reinterpret_cast<float*>(ws + p.off_dwf);
   int* counters = reinterpret_cast<int*>(ws + p.off_cnt);
   __nv_bfloat16* dz0 = reinterpret_cast<__nv_bfloat16*>(ws + p.off_dz);
-  __nv_bfloat16* dz1 = dz0 + static_cast<size_t>(p.Nb) * p.Vb;
+  __nv_bfloat16* dz1 = dz0 + static_cast<size_t>(p.Nb) * p.dz_ld;
   const bool dx_final = p.v_blocks == 1;
   const bool dw_final = !p.multi_n;
   FLCE_CUDA(cudaMemsetAsync(counters, 0, static_cast<size_t>(p.launches) * 4, s));
@@ -356,13 +398,19 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
       !make_tmap(&maps.w_k, W, H, V, H * 2, kBK, kHalfN) ||
       !make_tmap(&maps.w_mn, W, H, V, H * 2, 64, 64) ||
       !make_tmap(&maps.x_mn, X, H, N, H * 2, 64, 64) ||
-      !make_tmap(&maps.dz_k[0], dz0, p.Vb, p.Nb, p.Vb * 2, kBK, kBM) ||
-      !make_tmap(&maps.dz_k[1], dz1, p.Vb, p.Nb, p.Vb * 2, kBK, kBM) ||
-      !make_tmap(&maps.dz_mn[0], dz0, p.Vb, p.Nb, p.Vb * 2, 64, 64) ||
-      !make_tmap(&maps.dz_mn[1], dz1, p.Vb, p.Nb, p.Vb * 2, 64, 64) ||
-      !make_tmap(&maps.dz_st[0], dz0, p.Vb, p.Nb, p.Vb * 2, 64, 32) ||
-      !make_tmap(&maps.dz_st[1], dz1, p.Vb, p.Nb, p.Vb * 2, 64, 32))
+      !make_tmap(&maps.dz_k[0], dz0, p.Vb, p.Nb, p.dz_ld * 2, kBK, kBM) ||
+      !make_tmap(&maps.dz_k[1], dz1, p.Vb, p.Nb, p.dz_ld * 2, kBK, kBM) ||
+      !make_tmap(&maps.dz_mn[0], dz0, p.Vb, p.Nb, p.dz_ld * 2, 64, 64) ||
+      !make_tmap(&maps.dz_mn[1], dz1, p.Vb, p.Nb, p.dz_ld * 2, 64, 64) ||
+      !make_tmap(&maps.dz_st[0], dz0, p.Vb, p.Nb, p.dz_ld * 2, 64, 32) ||
+      !make_tmap(&maps.dz_st[1], dz1, p.Vb, p.Nb, p.dz_ld * 2, 64, 32))
     return FLCE_ERR_CUDA;
+  if (!make_tmap_mn3(&maps.dz_mn3[0], dz0, p.Vb, p.Nb, p.dz_ld * 2) ||
+      !make_tmap_mn3(&maps.dz_mn3[1], dz1, p.Vb, p.Nb, p.dz_ld * 2))
+    return FLCE_ERR_CUDA;
+  const bool mn3d = H % 64 == 0 && make_tmap_mn3(&maps.w_mn3, W, H, V, H * 2) &&
+                    make_tmap_mn3(&maps.x_mn3, X, H, N, H * 2);
+  if (!mn3d) maps.w_mn3 = maps.x_mn3 = maps.dz_mn3[0];  // unused
   // epilogue targets: FP32 accumulators (reduce-add, 32 x 32 boxes) or the bf16
   // gradients written directly (64 x 32 boxes); an unused map repeats a valid one
   constexpr CUtensorMapDataType kF32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -400,6 +448,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
   BwdArgs base;
   std::memset(&base, 0, sizeof(base));
   base.kb_h = static_cast<int>(cdiv(H, kBK));
+  base.mn3d = mn3d ? 1 : 0;
   base.N = static_cast<int>(N);
   base.H = static_cast<int>(H);
   base.V = static_cast<int>(V);
@@ -407,7 +456,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
   base.lse = lse;
   base.dz[0] = dz0;
   base.dz[1] = dz1;
-  base.dz_ld = static_cast<int>(p.Vb);
+  base.dz_ld = static_cast<int>(p.dz_ld);
   if (dX) {
     if (dx_final)
       base.dx_final = static_cast<__nv_bfloat16*>(dX);
@@ -436,6 +485,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
       a.r_tiles = a.r.mt * a.r.vt;
     }
     int xw_vb = -1, xw_nb = -1;
+    bool overlap = lp >= 1;  // directly after the previous backward launch
     if (lp >= 1) {
       const int b = lp - 1;
       a.xw = block(b);
@@ -443,11 +493,16 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
       xw_nb = b % p.n_blocks;
       if (dW) a.w_tiles = a.xw.vt * p.h_tiles;
       if (dX) a.x_tiles = a.xw.mt * p.h_tiles;
-      if (dW && !dw_final && xw_nb == 0)
+      if (dW && !dw_final && xw_nb == 0) {
         FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.xw.vt) * kBN * H * 4, s));
+        overlap = false;
+      }
     }
+    if (dW && !dw_final && lp >= 2 && (lp - 2) % p.n_blocks == p.n_blocks - 1)
+      overlap = false;  // a band downcast sits between this launch and the previous one
     const int tiles = a.r_tiles + a.w_tiles + a.x_tiles;
-    FLCE_CUDA(profiled(1, s, [&] { return launch_bwd_gemm(maps, a, tiles, s); }));
+    if (lp == 0) prof_begin(s);
+    FLCE_CUDA(launch_bwd_gemm(maps, a, tiles, overlap, s));
     if (dW && !dw_final && lp >= 1 && xw_nb == p.n_blocks - 1) {
       const int64_t col0 = int64_t{xw_vb} * p.Vb;
       const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
@@ -455,6 +510,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
                                 static_cast<size_t>(vext) * H, grad_loss, nv, red, s));
     }
   }
+  prof_end(1, nblk + 1, s);
   if (dX && !dx_final)
     FLCE_CUDA(launch_downcast(dxf, static_cast<__nv_bfloat16*>(dX), static_cast<size_t>(N) * H,
                               grad_loss, nv, red, s));
@@ -490,7 +546,7 @@ flce_status flce_profile_collect(double* ms, int64_t* launches) {
       st = FLCE_ERR_CUDA;
     if (r.kind >= 0 && r.kind < 4) {
       if (ms) ms[r.kind] += t;
-      if (launches) launches[r.kind] += 1;
+      if (launches) launches[r.kind] += r.launches;
     }
     g_event_pool.push_back(r.a);
     g_event_pool.push_back(r.b);

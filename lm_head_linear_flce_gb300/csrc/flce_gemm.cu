@@ -163,28 +163,41 @@ __device__ void pair_teardown(uint32_t tmem, int warp) {
 // ------------------------------------------------------- k-block operand loads
 // Each CTA loads its own 128 A rows and 128 B columns; completion is counted
 // on the leader's barrier `full` (a shared::cluster address).
-// Z = X W^T (FWD and R): both K-major.
+// Z = X W^T (FWD and R): both K-major.  X, re-read for every vocab tile, is
+// kept in L2 with an evict-last hint.
 __device__ __forceinline__ void load_xw(const CUtensorMap* tx, const CUtensorMap* tw, uint32_t sa,
-                                        uint32_t sb, int k, int arow, int brow, uint32_t full) {
-  tma_load_2d_pair(sa, tx, k, arow, full);
+                                        uint32_t sb, int k, int arow, int brow, uint32_t full,
+                                        uint64_t keep) {
+  tma_load_2d_pair_hint(sa, tx, k, arow, full, keep);
   tma_load_2d_pair(sb, tw, k, brow, full);
 }
 // dX tile: A = dZ rows (K-major over vocab), B = W rows of the block (MN-major over H).
 __device__ __forceinline__ void load_dx(const CUtensorMap* tdz, const CUtensorMap* twmn,
-                                        uint32_t sa, uint32_t sb, int k, int arow, int h0,
-                                        int vrow0, uint32_t full) {
+                                        const CUtensorMap* twmn3, bool mn3d, uint32_t sa,
+                                        uint32_t sb, int k, int arow, int h0, int vrow0,
+                                        uint32_t full) {
   tma_load_2d_pair(sa, tdz, k, arow, full);
+  if (mn3d) {
+    tma_load_3d_pair(sb, twmn3, 0, vrow0 + k, h0 / 64, full);
+  } else {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) tma_load_2d_pair(sb + q * 8192, twmn, h0 + 64 * q, vrow0 + k, full);
+    for (int q = 0; q < 2; ++q)
+      tma_load_2d_pair(sb + q * 8192, twmn, h0 + 64 * q, vrow0 + k, full);
+  }
 }
 // dW tile: A = dZ^T (MN-major over vocab), B = X rows of the block (MN-major over H).
 __device__ __forceinline__ void load_dw(const CUtensorMap* tdzmn, const CUtensorMap* txmn,
-                                        uint32_t sa, uint32_t sb, int k, int v0, int h0,
-                                        int trow0, uint32_t full) {
+                                        const CUtensorMap* tdzmn3, const CUtensorMap* txmn3,
+                                        bool mn3d, uint32_t sa, uint32_t sb, int k, int v0,
+                                        int h0, int trow0, uint32_t full, uint64_t keep) {
+  tma_load_3d_pair(sa, tdzmn3, 0, k, v0 / 64, full);  // the dZ slot is always 64-aligned
+  if (mn3d) {
+    tma_load_3d_pair_hint(sb, txmn3, 0, trow0 + k, h0 / 64, full, keep);
+  } else {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) tma_load_2d_pair(sa + q * 8192, tdzmn, v0 + 64 * q, k, full);
-#pragma unroll
-  for (int q = 0; q < 2; ++q) tma_load_2d_pair(sb + q * 8192, txmn, h0 + 64 * q, trow0 + k, full);
+    for (int q = 0; q < 2; ++q)
+      tma_load_2d_pair_hint(sb + q * 8192, txmn, h0 + 64 * q, trow0 + k, full, keep);
+  }
 }
 
 // ------------------------------------------------------- MMA of one k-block
@@ -290,10 +303,11 @@ struct Stager {
     }
     cur ^= 1u;
   }
+  // the FP32 accumulators are streamed through L2 once per block: evict first
   __device__ void reduce_add(int lane, const CUtensorMap* m, int x, int y) {
     publish();
     if (lane == 0) {
-      tma_reduce_add_2d(m, buf(), x, y);
+      tma_reduce_add_2d_hint(m, buf(), x, y, l2_policy_evict_first());
       bulk_commit();
     }
     cur ^= 1u;
@@ -442,6 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       Ring pipe;
       uint32_t issued = 0;
+      const uint64_t keep = l2_policy_evict_last();
       FwdSeq seq;
       for (seq.begin(); seq.valid(a); seq.next(a)) {
         const int arow = seq.mt(a) * kPairM + kBM * rank;
@@ -454,7 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (leader) mbar_arrive_expect_tx(full, kStageTx);
           load_xw(&tma_x, &tma_w, s.a_base + pipe.idx * kAStageBytes,
                   s.b_base + pipe.idx * kBStageBytes, kb * kBK, arow, brow,
-                  mapa_shared(full, 0));
+                  mapa_shared(full, 0), keep);
           issued |= 1u << pipe.idx;
           pipe.advance<kStages>();
         }
@@ -545,13 +560,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int total = a.w_tiles + a.r_tiles + a.x_tiles;
   const uint32_t tmem = pair_setup(s, warp);
   const WaitCtx w{s.abort_flag, a.err, a.wait_limit_ns};
+  // The next backward launch may start on SMs this grid frees.  It runs its
+  // recompute mainloops at once and waits for this grid before it touches the
+  // dZ slots (griddep_wait below).
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
       Ring pipe, ring;
       uint32_t issued = 0;
+      bool prior_done = false;  // the preceding grid (which wrote this dZ slot) has completed
+      const uint64_t keep = l2_policy_evict_last();
       const CUtensorMap* dz_k = &maps.dz_k[a.xw.slot & 1];
       const CUtensorMap* dz_mn = &maps.dz_mn[a.xw.slot & 1];
+      const CUtensorMap* dz_mn3 = &maps.dz_mn3[a.xw.slot & 1];
+      const bool mn3d = a.mn3d != 0;
       for (;;) {
         int t;
         if (leader) {
@@ -571,6 +594,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         ring.advance<kTicketRing>();
         if (t >= total) break;
         const Tile tile = decode_ticket(a, t);
+        if (tile.kind != kKindR && !prior_done) {
+          griddep_wait();
+          prior_done = true;
+        }
         const int arow = tile.m0 + kBM * rank;     // this CTA's A rows (M)
         const int bcol = tile.n0 + kHalfN * rank;  // this CTA's B columns (N)
         bool ok = true;
@@ -584,11 +611,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const int k = kb * kBK;
           if (leader) mbar_arrive_expect_tx(full, kStageTx);
           if (tile.kind == kKindR)
-            load_xw(&maps.x_k, &maps.w_k, sa, sb, k, a.r.row0 + arow, a.r.col0 + bcol, full_c);
+            load_xw(&maps.x_k, &maps.w_k, sa, sb, k, a.r.row0 + arow, a.r.col0 + bcol, full_c,
+                    keep);
           else if (tile.kind == kKindX)
-            load_dx(dz_k, &maps.w_mn, sa, sb, k, arow, bcol, a.xw.col0, full_c);
+            load_dx(dz_k, &maps.w_mn, &maps.w_mn3, mn3d, sa, sb, k, arow, bcol, a.xw.col0,
+                    full_c);
           else
-            load_dw(dz_mn, &maps.x_mn, sa, sb, k, arow, bcol, a.xw.row0, full_c);
+            load_dw(dz_mn, &maps.x_mn, dz_mn3, &maps.x_mn3, mn3d, sa, sb, k, arow, bcol,
+                    a.xw.row0, full_c, keep);
           issued |= 1u << pipe.idx;
           pipe.advance<kStages>();
         }
@@ -631,6 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     Stager st;
     st.buf0 = s.staging + static_cast<uint32_t>(q) * 2 * kStageBufBytes;
     Ring accr, ring;
+    bool prior_done = false;  // no dZ store before the preceding grid has completed
     for (;;) {
       if (!wait_parity_cluster(s.qfull + 8 * ring.idx, ring.phase, w)) break;
       const int t = s.tickets_p[ring.idx];
@@ -650,6 +681,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (!wait_parity(s.tfull + 8 * accr.idx, accr.phase, w)) break;
+      if (!prior_done) {
+        griddep_wait();
+        prior_done = true;
+      }
       tc_fence_after();
       const uint32_t tbase =
           tmem + (static_cast<uint32_t>(q * 32) << 16) + accr.idx * kAccCols;
@@ -730,7 +765,8 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const 
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, cudaStream_t st) {
+cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, bool overlap_prior,
+                            cudaStream_t st) {
   if (units <= 0) return cudaSuccess;
   static bool attr = false;
   static int pairs = 0;
@@ -743,9 +779,19 @@ cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, cu
   }
   const int n = std::min(units, max_pairs(reinterpret_cast<const void*>(flce_bwd_kernel),
                                           kBwdSmemBytes, &pairs));
-  flce_bwd_kernel<<<2 * n, kGemmThreads, kBwdSmemBytes, st>>>(maps, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * n, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kBwdSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl;
+  cfg.numAttrs = overlap_prior ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, flce_bwd_kernel, maps, a);
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace flce

@@ -73,6 +73,12 @@ struct BwdMaps {
   CUtensorMap x_mn;      // X [N][H], box 64 x 64  (W: B operand, MN-major)
   CUtensorMap dz_k[2];   // dZ slot [Nb][Vb], box 64 x 128 (X: A operand)
   CUtensorMap dz_mn[2];  // dZ slot [Nb][Vb], box 64 x 64  (W: A operand, MN-major)
+  // MN-major operand halves as one box each: a 3-D view (64 elements, rows,
+  // 64-element groups) with box 64 x 64 rows x 2 groups lands in shared memory
+  // exactly as two 64 x 64 boxes 8 KB apart.  Used when H % 64 == 0.
+  CUtensorMap w_mn3;     // W  (64, V, H/64)
+  CUtensorMap x_mn3;     // X  (64, N, H/64)
+  CUtensorMap dz_mn3[2]; // dZ slot (64, Nb, Vb/64)
   // epilogue stores, box = one warp's 32 rows x 128 bytes
   CUtensorMap dz_st[2];  // dZ slot [Nb][Vb] bf16, box 64 x 32 (R: dZ store)
   CUtensorMap dx_out;    // dX accumulator [N][H] f32 box 32 x 32 (reduce-add), or
@@ -86,6 +92,7 @@ struct BwdArgs {
   BlockDesc r, xw;
   int r_tiles, w_tiles, x_tiles;
   int kb_h;  // K blocks of the recompute (ceil(H / 64))
+  int mn3d;  // 1: MN-major halves load as one 3-D box (w_mn3 / x_mn3 / dz_mn3)
   int N, H, V;
   const int* targets;
   const float* lse;
@@ -109,6 +116,7 @@ struct Plan {
   int64_t N, H, V;
   int m_tiles, v_tiles, v_units, h_tiles;
   int64_t Nb, Vb;         // backward block: token rows x vocab columns
+  int64_t dz_ld;          // elements per dZ row in a slot (Vb plus padding)
   int n_blocks, v_blocks;
   bool multi_n;           // more than one token block: dW needs an FP32 band
   int launches;           // backward GEMM launches (one per dZ block, plus one)
@@ -139,6 +147,9 @@ cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* err, cudaStre
 // fit on the device at once.
 cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const GemmArgs& a,
                             int units, cudaStream_t st);
-cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, cudaStream_t st);
+// overlap_prior: the preceding operation of the stream is the previous backward
+// launch, which this one may overlap (programmatic dependent launch).
+cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, bool overlap_prior,
+                            cudaStream_t st);
 
 }  // namespace flce
