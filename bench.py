@@ -48,6 +48,42 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_qwen2_7b.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "lm_head_linear_flce_gb300", "csrc", f)
+                  for f in ("flce_gemm.cu", "flce_api.cu")]
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload: str, kind: str):
+    """DRAM bytes per launch of `kind` from the committed ncu capture, or None
+    when the capture is for another workload or the kernel sources changed."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            text = f.read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("workload") != workload or vals.get("sources") != kernel_source_digest():
+        return None
+    try:
+        return int(float(vals[f"{kind}_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -200,40 +236,61 @@ def run_ours(args, world, rank, local):
     value, worst = aggregate_throughput(N, args.steps, elapsed, world, dev)
     ms_step = worst / args.steps
 
-    # end to end through the public autograd call, inputs from pinned host memory
+    # End to end through the public autograd call.  Every step copies its inputs
+    # from pinned host memory and reads the loss back; the copy of step i+1 runs
+    # on a second stream while step i computes (double-buffered device inputs),
+    # as a training loop that prefetches its next batch would.
     e2e = None
     if not args.no_e2e:
-        Xd = torch.empty_like(X)
-        Wd = torch.empty_like(W)
-        Ld = torch.empty_like(L)
-        loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
-        e_steps = max(1, min(args.steps, 5))
+        del ws
+        torch.cuda.empty_cache()
+        bufs = [(torch.empty_like(X), torch.empty_like(W), torch.empty_like(L)) for _ in range(2)]
+        loss_h = torch.empty(max(1, args.steps), dtype=torch.float32).pin_memory()
+        copy_stream = torch.cuda.Stream(dev)
+        copied = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+        e_steps = max(1, min(args.steps, 8))
 
-        def e2e_step():
-            Xd.copy_(Xh, non_blocking=True)
-            Wd.copy_(Wh, non_blocking=True)
-            Ld.copy_(Lh, non_blocking=True)
-            xg = Xd.detach().requires_grad_(True)
-            wg = Wd.detach().requires_grad_(True)
-            lo = flce.linear_cross_entropy(xg, wg, Ld, shift=wl.shift, reduction=wl.reduction,
-                                           seq_len=wl.S)
-            lo.backward()
-            loss_h.copy_(lo.detach().reshape(1), non_blocking=True)
+        def issue_copy(i):
+            b = i % 2
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(consumed[b])
+                for d, h in zip(bufs[b], (Xh, Wh, Lh)):
+                    d.copy_(h, non_blocking=True)
+                copied[b].record(copy_stream)
 
-        e2e_step()
+        def e2e_run(n):
+            for b in range(2):
+                consumed[b].record(stream)
+            issue_copy(0)
+            for i in range(n):
+                b = i % 2
+                stream.wait_event(copied[b])
+                if i + 1 < n:
+                    issue_copy(i + 1)
+                Xd, Wd, Ld = bufs[b]
+                xg = Xd.detach().requires_grad_(True)
+                wg = Wd.detach().requires_grad_(True)
+                lo = flce.linear_cross_entropy(xg, wg, Ld, shift=wl.shift,
+                                               reduction=wl.reduction, seq_len=wl.S)
+                lo.backward()
+                loss_h[i].copy_(lo.detach(), non_blocking=True)
+                consumed[b].record(stream)
+
+        e2e_run(2)
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(e_steps):
-            e2e_step()
+        e2e_run(e_steps)
         e1.record(stream)
         torch.cuda.synchronize()
         e_val, _ = aggregate_throughput(N, e_steps, e0.elapsed_time(e1), world, dev)
         h2d = X.numel() * 2 + W.numel() * 2 + L.numel() * 8
-        e2e = {"value": e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": round(e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": 4, "steps": e_steps,
-               "api": "lm_head_linear_flce_gb300.linear_cross_entropy + backward"}
+               "api": "lm_head_linear_flce_gb300.linear_cross_entropy + backward",
+               "copies": "inputs of step i+1 copied on a second stream during step i"}
 
     peaks, src = load_peaks()
     flops = wl.flops
@@ -250,7 +307,8 @@ def run_ours(args, world, rank, local):
     step_ms_total = sum(v[0] for v in kinds.values())
     roofline = {
         "kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-        "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+        "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+        "traffic": load_traffic(wl.name, dom),
         "peak_source": f"bf16_tflops_sustained ({src})",
         "launches_per_step": dom_n / args.steps,
         "avg_launch_ms": dom_ms / dom_n,
