@@ -179,3 +179,35 @@ def test_repeat_calls_are_stable():
     b = run_case(X, W, labels)
     assert a["loss"] == b["loss"]  # deterministic loss reduction
     np.testing.assert_array_equal(a["lse"], b["lse"])
+
+
+@pytest.mark.parametrize("H", [8, 16, 32, 40])
+def test_small_hidden_sizes(H):
+    X, W, labels = workloads.random_case(300, H, 700, seed=20 + H, w_std=0.3)
+    check_against_oracle(X, W, labels, grad=1.5)
+
+
+def test_single_class_vocabulary():
+    # V = 1: softmax is 1 everywhere, so every valid row has loss 0 and no gradient
+    X, W, labels = workloads.random_case(200, 64, 1, seed=30, ignore_frac=0.2)
+    got, ref = check_against_oracle(X, W, labels)
+    assert abs(got["loss"]) < 1e-6
+    assert not got["dX"].any() and not got["dW"].any()
+
+
+def test_shift_with_length_one_sequences_ignores_everything():
+    X, W, labels = workloads.random_case(128, 64, 300, seed=31, ignore_frac=0.0)
+    got, ref = check_against_oracle(X, W, labels, seq_len=1, shift=True)
+    assert got["n_valid"] == 0 and got["loss"] == 0.0
+
+
+def test_default_blocking_several_token_blocks():
+    # N above 8192 rows: two token blocks with the default backward blocking,
+    # so dW accumulates in the FP32 band and dX over several vocab blocks
+    X, W, labels = workloads.random_case(8192 + 300, 64, 9000, seed=32, w_std=0.2)
+    check_against_oracle(X, W, labels, seq_len=8492, shift=True)
+
+
+def test_many_vocab_blocks_few_rows():
+    X, W, labels = workloads.random_case(96, 128, 70000, seed=33, w_std=0.1)
+    check_against_oracle(X, W, labels, reduction="sum")
