@@ -116,6 +116,29 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels,
                           void* workspace, size_t workspace_bytes, flce_stream_t stream);
 
 /*
+ * Backward with dW accumulated into an existing FP32 gradient:
+ *
+ *   dW_acc[V][H] += s * dZ^T X        (s = g / n_valid for mean, g for sum)
+ *
+ * for a weight whose gradient has other contributions too, e.g. an LM head
+ * tied to the input embedding, or gradient accumulation over micro-batches
+ * (Megatron-LM PR #2739, section 1: the fused loss must feed the output
+ * layer's own weight gradient).  dW_acc: device float [V][H], 16-byte
+ * aligned, read and written (not overwritten).  dX (bf16 or NULL) and the
+ * other arguments are as in flce_backward.  The FP32 additions into dW_acc and
+ * into the internal dX accumulator happen in a fixed order (one per vocab /
+ * token block, in launch order), so repeated calls give bitwise-identical
+ * results.
+ */
+flce_status flce_backward_accumulate(const void* X, const void* W, const int64_t* labels,
+                                     int64_t N, int64_t H, int64_t V, int64_t seq_len,
+                                     int64_t ignore_index, int shift, flce_reduction reduction,
+                                     const float* lse, const int64_t* n_valid,
+                                     const float* grad_loss, void* dX, float* dW_acc,
+                                     void* workspace, size_t workspace_bytes,
+                                     flce_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and returns the device error word written
  * by the last flce_forward / flce_backward call that used this workspace:
  * FLCE_OK, FLCE_ERR_LABEL_OUT_OF_RANGE or FLCE_ERR_TIMEOUT (the first one

@@ -22,7 +22,7 @@ __all__ = [
     "FlceError", "library", "library_path", "workspace_size", "flce_forward", "flce_backward",
     "flce_get_error", "flce_selftest_wait_timeout", "flce_set_wait_limit_ns",
     "flce_set_backward_block", "flce_kernel_launch_count", "flce_profile_enable",
-    "flce_profile_collect", "PROFILE_KINDS", "flce_forward_noalloc",
+    "flce_profile_collect", "PROFILE_KINDS", "flce_forward_noalloc", "flce_backward_accumulate",
     "linear_cross_entropy", "STATUS",
 ]
 
@@ -167,6 +167,34 @@ def flce_backward(X, W, labels, lse, n_valid, grad_loss, *, seq_len=None, ignore
                                  _ptr(ws), ws.numel(), _stream(dev))
     _check(st, "flce_backward")
     return (dX if need_dX else None), (dW if need_dW else None), ws
+
+
+def flce_backward_accumulate(X, W, labels, lse, n_valid, grad_loss, dW_acc, *, seq_len=None,
+                             ignore_index=-100, shift=False, reduction="mean", need_dX=True,
+                             workspace=None, dX=None):
+    """Calls flce_backward_accumulate: dW_acc (float32 [V, H], modified in place)
+    += the weight gradient; returns (dX or None, workspace)."""
+    _check_inputs(X, W, labels)
+    N, H = X.shape
+    V = W.shape[0]
+    if dW_acc.dtype != torch.float32 or tuple(dW_acc.shape) != (V, H) or not dW_acc.is_contiguous():
+        raise ValueError("dW_acc must be a contiguous float32 [V, H] tensor")
+    dev = X.device
+    ws = _workspace(N, H, V, dev, workspace)
+    if need_dX and dX is None:
+        dX = torch.empty_like(X)
+    g = grad_loss.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+    lib = library()
+    fn = lib.flce_backward_accumulate
+    c_i64, c_p, c_int, c_sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    fn.argtypes = [c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i64, c_i64, c_int, c_int,
+                   c_p, c_p, c_p, c_p, c_p, c_p, c_sz, c_p]
+    fn.restype = c_int
+    st = fn(_ptr(X), _ptr(W), _ptr(labels), N, H, V, int(seq_len or 0), int(ignore_index),
+            int(bool(shift)), _REDUCTION[reduction], _ptr(lse), _ptr(n_valid), _ptr(g),
+            _ptr(dX if need_dX else None), _ptr(dW_acc), _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "flce_backward_accumulate")
+    return (dX if need_dX else None), ws
 
 
 def flce_get_error(workspace) -> int:

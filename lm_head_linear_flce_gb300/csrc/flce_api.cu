@@ -353,17 +353,24 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   return FLCE_OK;
 }
 
-flce_status flce_backward(const void* X, const void* W, const int64_t* labels, int64_t N,
+}  // extern "C"
+
+namespace {
+
+// Shared body of flce_backward (dW written as bf16) and
+// flce_backward_accumulate (dW_acc += scale * dZ^T X in FP32).
+flce_status backward_impl(const void* X, const void* W, const int64_t* labels, int64_t N,
                           int64_t H, int64_t V, int64_t seq_len, int64_t ignore_index, int shift,
                           flce_reduction reduction, const float* lse, const int64_t* n_valid,
-                          const float* grad_loss, void* dX, void* dW, void* workspace,
-                          size_t workspace_bytes, flce_stream_t stream) {
+                          const float* grad_loss, void* dX, void* dW, float* dW_acc,
+                          void* workspace, size_t workspace_bytes, flce_stream_t stream) {
   Plan p;
   flce_status st = check_common(X, W, labels, N, H, V, seq_len, shift, reduction, workspace,
                                 workspace_bytes, &p);
   if (st != FLCE_OK) return st;
   if (!n_valid || !grad_loss || (N > 0 && !lse)) return FLCE_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(dX) | reinterpret_cast<uintptr_t>(dW)) & 15)
+  if ((reinterpret_cast<uintptr_t>(dX) | reinterpret_cast<uintptr_t>(dW) |
+       reinterpret_cast<uintptr_t>(dW_acc)) & 15)
     return FLCE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLCE_OK) return st;
@@ -373,9 +380,10 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
   FLCE_CUDA(cudaMemsetAsync(err, 0, 16, s));
   if (N == 0) {
     if (dW) FLCE_CUDA(cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 2, s));
-    return FLCE_OK;
+    return FLCE_OK;  // nothing to add to dW_acc
   }
-  if (!dX && !dW) return FLCE_OK;
+  const bool want_dw = dW || dW_acc;
+  if (!dX && !want_dw) return FLCE_OK;
   const int red = reduction == FLCE_REDUCTION_SUM ? 1 : 0;
   const long long* nv = reinterpret_cast<const long long*>(n_valid);
   int* targets = reinterpret_cast<int*>(ws + p.off_t);
@@ -390,6 +398,7 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
   __nv_bfloat16* dz1 = dz0 + static_cast<size_t>(p.Nb) * p.dz_ld;
   const bool dx_final = p.v_blocks == 1;
   const bool dw_final = !p.multi_n;
+  const bool band = dW && !dw_final;  // bf16 dW over several token blocks: FP32 band
   FLCE_CUDA(cudaMemsetAsync(counters, 0, static_cast<size_t>(p.launches) * 4, s));
   if (dX && !dx_final) FLCE_CUDA(cudaMemsetAsync(dxf, 0, static_cast<size_t>(N) * H * 4, s));
 
@@ -421,7 +430,9 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
     ok = make_tmap(&maps.dx_out, dxf, H, N, H * 4, 32, 32, kF32);
   else
     maps.dx_out = maps.dz_st[0];
-  if (ok && dW && dw_final)
+  if (ok && dW_acc)
+    ok = make_tmap(&maps.dw_out, dW_acc, H, V, H * 4, 32, 32, kF32);
+  else if (ok && dW && dw_final)
     ok = make_tmap(&maps.dw_out, dW, H, V, H * 2, 64, 32);
   else if (ok && dW)
     ok = make_tmap(&maps.dw_out, dwf, H, p.Vb, H * 4, 32, 32, kF32);
@@ -463,7 +474,9 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
     else
       base.dxf = dxf;
   }
-  if (dW) {
+  if (dW_acc) {
+    base.dw_accumulate = 1;
+  } else if (dW) {
     if (dw_final)
       base.dw_final = static_cast<__nv_bfloat16*>(dW);
     else
@@ -491,19 +504,19 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
       a.xw = block(b);
       xw_vb = b / p.n_blocks;
       xw_nb = b % p.n_blocks;
-      if (dW) a.w_tiles = a.xw.vt * p.h_tiles;
+      if (want_dw) a.w_tiles = a.xw.vt * p.h_tiles;
       if (dX) a.x_tiles = a.xw.mt * p.h_tiles;
-      if (dW && !dw_final && xw_nb == 0) {
+      if (band && xw_nb == 0) {
         FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.xw.vt) * kBN * H * 4, s));
         overlap = false;
       }
     }
-    if (dW && !dw_final && lp >= 2 && (lp - 2) % p.n_blocks == p.n_blocks - 1)
+    if (band && lp >= 2 && (lp - 2) % p.n_blocks == p.n_blocks - 1)
       overlap = false;  // a band downcast sits between this launch and the previous one
     const int tiles = a.r_tiles + a.w_tiles + a.x_tiles;
     if (lp == 0) prof_begin(s);
     FLCE_CUDA(launch_bwd_gemm(maps, a, tiles, overlap, s));
-    if (dW && !dw_final && lp >= 1 && xw_nb == p.n_blocks - 1) {
+    if (band && lp >= 1 && xw_nb == p.n_blocks - 1) {
       const int64_t col0 = int64_t{xw_vb} * p.Vb;
       const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
       FLCE_CUDA(launch_downcast(dwf, static_cast<__nv_bfloat16*>(dW) + col0 * H,
@@ -515,6 +528,32 @@ flce_status flce_backward(const void* X, const void* W, const int64_t* labels, i
     FLCE_CUDA(launch_downcast(dxf, static_cast<__nv_bfloat16*>(dX), static_cast<size_t>(N) * H,
                               grad_loss, nv, red, s));
   return FLCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+flce_status flce_backward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                          int64_t H, int64_t V, int64_t seq_len, int64_t ignore_index, int shift,
+                          flce_reduction reduction, const float* lse, const int64_t* n_valid,
+                          const float* grad_loss, void* dX, void* dW, void* workspace,
+                          size_t workspace_bytes, flce_stream_t stream) {
+  return backward_impl(X, W, labels, N, H, V, seq_len, ignore_index, shift, reduction, lse,
+                       n_valid, grad_loss, dX, dW, nullptr, workspace, workspace_bytes, stream);
+}
+
+flce_status flce_backward_accumulate(const void* X, const void* W, const int64_t* labels,
+                                     int64_t N, int64_t H, int64_t V, int64_t seq_len,
+                                     int64_t ignore_index, int shift, flce_reduction reduction,
+                                     const float* lse, const int64_t* n_valid,
+                                     const float* grad_loss, void* dX, float* dW_acc,
+                                     void* workspace, size_t workspace_bytes,
+                                     flce_stream_t stream) {
+  if (!dW_acc) return FLCE_ERR_INVALID_ARG;
+  return backward_impl(X, W, labels, N, H, V, seq_len, ignore_index, shift, reduction, lse,
+                       n_valid, grad_loss, dX, nullptr, dW_acc, workspace, workspace_bytes,
+                       stream);
 }
 
 flce_status flce_get_error(const void* workspace, flce_stream_t stream) {

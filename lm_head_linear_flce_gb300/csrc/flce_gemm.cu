@@ -347,9 +347,11 @@ __device__ __forceinline__ void epi_dz_staged(uint32_t tbase, int gcol0, int V, 
   }
 }
 
-// FP32 accumulator rows: reduce-add 32 columns per chunk into the FP32 buffer.
-__device__ __forceinline__ void epi_reduce_staged(uint32_t tbase, int h0, int H, Stager& st,
-                                                  int lane, const CUtensorMap* m, int y) {
+// FP32 accumulator rows: reduce-add scale * value, 32 columns per chunk, into
+// an FP32 buffer.
+__device__ __forceinline__ void epi_reduce_staged(uint32_t tbase, int h0, int H, float scale,
+                                                  Stager& st, int lane, const CUtensorMap* m,
+                                                  int y) {
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     const int h = h0 + 32 * c;
@@ -358,7 +360,7 @@ __device__ __forceinline__ void epi_reduce_staged(uint32_t tbase, int h0, int H,
     tmem_ld32(tbase + 32 * c, v);
     uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(scale * v[i]);
     st.acquire(lane);
     st.write_row(lane, w);
     st.reduce_add(lane, m, h, y);
@@ -656,8 +658,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     const int r = kBM * rank + q * 32 + lane;  // row of the 256-row tile
     // scale g / n_valid (mean) or g (sum), applied when a tile writes bf16 directly
-    const float scale =
-        (a.dx_final || a.dw_final) ? grad_scale(a.grad_loss, a.n_valid, a.reduction) : 1.f;
+    const float scale = (a.dx_final || a.dw_final || a.dw_accumulate)
+                            ? grad_scale(a.grad_loss, a.n_valid, a.reduction)
+                            : 1.f;
     Stager st;
     st.buf0 = s.staging + static_cast<uint32_t>(q) * 2 * kStageBufBytes;
     Ring accr, ring;
@@ -696,12 +699,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         if (a.dx_final)
           epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dx_out, a.xw.row0 + y0);
         else
-          epi_reduce_staged(tbase, tile.n0, a.H, st, lane, &maps.dx_out, a.xw.row0 + y0);
+          epi_reduce_staged(tbase, tile.n0, a.H, 1.f, st, lane, &maps.dx_out, a.xw.row0 + y0);
       } else {
         if (a.dw_final)
           epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dw_out, a.xw.col0 + y0);
         else
-          epi_reduce_staged(tbase, tile.n0, a.H, st, lane, &maps.dw_out, y0);
+          // an FP32 band (scaled later), or the caller's FP32 gradient (scaled here)
+          epi_reduce_staged(tbase, tile.n0, a.H, a.dw_accumulate ? scale : 1.f, st, lane,
+                            &maps.dw_out, a.dw_accumulate ? a.xw.col0 + y0 : y0);
       }
       tc_fence_before();
       __syncwarp();

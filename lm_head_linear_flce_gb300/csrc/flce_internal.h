@@ -102,6 +102,7 @@ struct BwdArgs {
   __nv_bfloat16* dx_final;     // bf16 dX written directly (single vocab block), or null
   float* dwf;                  // FP32 dW band [Vb][H], or null
   __nv_bfloat16* dw_final;     // bf16 dW written directly (single token block), or null
+  int dw_accumulate;           // 1: W tiles add scale * dW into the caller's FP32 gradient
   const float* grad_loss;
   const long long* n_valid;
   int reduction;               // 0 mean, 1 sum
