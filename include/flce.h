@@ -139,6 +139,21 @@ flce_status flce_backward_accumulate(const void* X, const void* W, const int64_t
                                      flce_stream_t stream);
 
 /*
+ * Plain logits, for calls without labels (inference / generation): the
+ * fused path falls back to the LM head itself, Z = X W^T (ms-swift PR #9784,
+ * section Safety & Compatibility: "labels=None" falls back to lm_head).
+ *
+ *   logits     device bf16 [N][ld_logits], row-major; columns [V, ld_logits)
+ *              are left untouched.  ld_logits >= V and a multiple of 8;
+ *              16-byte aligned.  Each value is the FP32 accumulation rounded
+ *              to bf16 (round to nearest even).
+ * Needs no workspace and holds N x V memory by definition (the caller asked
+ * for the logits).  Errors as for flce_forward.
+ */
+flce_status flce_logits(const void* X, const void* W, int64_t N, int64_t H, int64_t V,
+                        void* logits, int64_t ld_logits, flce_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and returns the device error word written
  * by the last flce_forward / flce_backward call that used this workspace:
  * FLCE_OK, FLCE_ERR_LABEL_OUT_OF_RANGE or FLCE_ERR_TIMEOUT (the first one

@@ -23,6 +23,7 @@ __all__ = [
     "flce_get_error", "flce_selftest_wait_timeout", "flce_set_wait_limit_ns",
     "flce_set_backward_block", "flce_kernel_launch_count", "flce_profile_enable",
     "flce_profile_collect", "PROFILE_KINDS", "flce_forward_noalloc", "flce_backward_accumulate",
+    "flce_logits",
     "linear_cross_entropy", "STATUS",
 ]
 
@@ -197,6 +198,26 @@ def flce_backward_accumulate(X, W, labels, lse, n_valid, grad_loss, dW_acc, *, s
     return (dX if need_dX else None), ws
 
 
+def flce_logits(X, W):
+    """Calls flce_logits: bf16 logits [N, V] = X W^T (no labels, no loss)."""
+    for name, t in (("hidden", X), ("weight", W)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous 2-D bf16 CUDA tensor")
+    N, H = X.shape
+    V = W.shape[0]
+    if W.shape[1] != H:
+        raise ValueError("shape mismatch between X and W")
+    ld = (V + 7) // 8 * 8
+    out = torch.empty(N, ld, dtype=torch.bfloat16, device=X.device)
+    lib = library()
+    fn = lib.flce_logits
+    c_i64, c_p = ctypes.c_int64, ctypes.c_void_p
+    fn.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_i64, c_p]
+    fn.restype = ctypes.c_int
+    _check(fn(_ptr(X), _ptr(W), N, H, V, _ptr(out), ld, _stream(X.device)), "flce_logits")
+    return out[:, :V] if ld != V else out
+
+
 def flce_get_error(workspace) -> int:
     """Synchronises the current stream and returns the workspace's error status."""
     return int(library().flce_get_error(_ptr(workspace), _stream(workspace.device)))
@@ -298,8 +319,14 @@ def linear_cross_entropy(hidden, weight, labels, ignore_index=-100, shift=False,
     or [N].  With shift=True, position s of each sequence is scored against
     labels[s+1] and the last position is ignored (for 3-D hidden the sequence
     length is S; for 2-D, seq_len or one sequence).  Returns a 0-dim float32
-    loss that back-propagates to hidden and weight.
+    loss that back-propagates to hidden and weight.  With labels=None it
+    returns the bf16 logits hidden @ weight.T instead (no gradient).
     """
+    if labels is None:
+        # no labels: the plain LM head (inference); returns bf16 logits
+        lead = hidden.shape[:-1]
+        Z = flce_logits(hidden.reshape(-1, hidden.shape[-1]).contiguous(), weight.contiguous())
+        return Z.reshape(*lead, weight.shape[0])
     if reduction not in _REDUCTION:
         raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
     if hidden.dim() == 3:

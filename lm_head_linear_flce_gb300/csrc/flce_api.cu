@@ -556,6 +556,38 @@ flce_status flce_backward_accumulate(const void* X, const void* W, const int64_t
                        stream);
 }
 
+flce_status flce_logits(const void* X, const void* W, int64_t N, int64_t H, int64_t V,
+                        void* logits, int64_t ld_logits, flce_stream_t stream) {
+  if (N < 0 || H <= 0 || V <= 0) return FLCE_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > kMaxH || N > kMaxDim || V > kMaxDim) return FLCE_ERR_UNSUPPORTED_SHAPE;
+  if (N == 0) return FLCE_OK;
+  if (!X || !W || !logits || ld_logits < V || ld_logits % 8 != 0) return FLCE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W) |
+       reinterpret_cast<uintptr_t>(logits)) & 15)
+    return FLCE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  flce_status st = device_info(&dev);
+  if (st != FLCE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CUtensorMap tx, tw, tout;
+  if (!make_tmap(&tx, X, H, N, H * 2, kBK, kBM) || !make_tmap(&tw, W, H, V, H * 2, kBK, kHalfN) ||
+      !make_tmap(&tout, logits, V, N, ld_logits * 2, 64, 32))
+    return FLCE_ERR_CUDA;
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.tiles_m = static_cast<int>(cdiv(N, kPairM));
+  a.tiles_n = static_cast<int>(cdiv(V, kBN));
+  a.group = kFwdGroup;
+  a.units = a.tiles_m * static_cast<int>(cdiv(a.tiles_n, kFwdGroup));
+  a.k_blocks = static_cast<int>(cdiv(H, kBK));
+  a.N = static_cast<int>(N);
+  a.H = static_cast<int>(H);
+  a.V = static_cast<int>(V);
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  FLCE_CUDA(launch_logits_gemm(tx, tw, tout, a, a.units, s));
+  return FLCE_OK;
+}
+
 flce_status flce_get_error(const void* workspace, flce_stream_t stream) {
   if (!workspace) return FLCE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

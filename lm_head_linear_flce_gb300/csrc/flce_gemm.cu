@@ -438,11 +438,19 @@ struct FwdSeq {
 
 }  // namespace
 
+// MODE kFwdLse: the forward of the loss (log-sum-exp epilogue).
+// MODE kFwdLogits: plain logits Z = X W^T rounded to bf16 and stored through
+// shared-memory staging (the inference path with no labels).
+constexpr int kFwdLse = 0;
+constexpr int kFwdLogits = 1;
+
+template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     flce_fwd_kernel(const __grid_constant__ CUtensorMap tma_x,
-                    const __grid_constant__ CUtensorMap tma_w, const GemmArgs a) {
+                    const __grid_constant__ CUtensorMap tma_w,
+                    const __grid_constant__ CUtensorMap tma_out, const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const Smem s = carve_smem(smem_raw, 0);
+  const Smem s = carve_smem(smem_raw, MODE == kFwdLogits ? 4 * 2 * kStageBufBytes : 0);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = static_cast<int>(cluster_ctarank());
@@ -492,6 +500,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       }
       drain_mma(s, w);
     }
+  } else if (MODE == kFwdLogits) {
+    const int q = warp & 3;
+    Stager st;
+    st.buf0 = s.staging + static_cast<uint32_t>(q) * 2 * kStageBufBytes;
+    Ring accr;
+    FwdSeq seq;
+    for (seq.begin(); seq.valid(a); seq.next(a)) {
+      const int y0 = seq.mt(a) * kPairM + kBM * rank + 32 * q;  // first row of this warp
+      const int n0 = seq.nt(a) * kBN;
+      if (!wait_parity(s.tfull + 8 * accr.idx, accr.phase, w)) break;
+      tc_fence_after();
+      const uint32_t tbase =
+          tmem + (static_cast<uint32_t>(q * 32) << 16) + accr.idx * kAccCols;
+      epi_final_staged(tbase, n0, a.V, 1.f, st, lane, &tma_out, y0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(s.tempty + 8 * accr.idx, 0));
+      accr.advance<kNumAcc>();
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = kBM * rank + q * 32 + lane;  // row of the 256-row tile
@@ -756,16 +785,36 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const 
   if (units <= 0) return cudaSuccess;
   static bool attr = false;
   static int pairs = 0;
+  auto* k = flce_fwd_kernel<kFwdLse>;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(flce_fwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGemmSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int n = std::min(units, max_pairs(reinterpret_cast<const void*>(flce_fwd_kernel),
-                                          kGemmSmemBytes, &pairs));
-  flce_fwd_kernel<<<2 * n, kGemmThreads, kGemmSmemBytes, st>>>(tx, tw, a);
+  const int n =
+      std::min(units, max_pairs(reinterpret_cast<const void*>(k), kGemmSmemBytes, &pairs));
+  k<<<2 * n, kGemmThreads, kGemmSmemBytes, st>>>(tx, tw, tx, a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_logits_gemm(const CUtensorMap& tx, const CUtensorMap& tw,
+                               const CUtensorMap& tout, const GemmArgs& a, int units,
+                               cudaStream_t st) {
+  if (units <= 0) return cudaSuccess;
+  static bool attr = false;
+  static int pairs = 0;
+  auto* k = flce_fwd_kernel<kFwdLogits>;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int n =
+      std::min(units, max_pairs(reinterpret_cast<const void*>(k), kBwdSmemBytes, &pairs));
+  k<<<2 * n, kGemmThreads, kBwdSmemBytes, st>>>(tx, tw, tout, a);
   note_launch();
   return cudaGetLastError();
 }

@@ -148,6 +148,9 @@ cudaError_t launch_selftest_wait(unsigned long long limit_ns, int* err, cudaStre
 // fit on the device at once.
 cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const GemmArgs& a,
                             int units, cudaStream_t st);
+cudaError_t launch_logits_gemm(const CUtensorMap& tx, const CUtensorMap& tw,
+                               const CUtensorMap& tout, const GemmArgs& a, int units,
+                               cudaStream_t st);
 // overlap_prior: the preceding operation of the stream is the previous backward
 // launch, which this one may overlap (programmatic dependent launch).
 cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, bool overlap_prior,
