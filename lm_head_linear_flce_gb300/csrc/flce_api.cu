@@ -245,6 +245,10 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   off = shared_start;
   p->off_cnt = off;
   off = align_up(off + static_cast<size_t>(p->launches) * 4);
+  p->off_flags = off;  // per 256-row token tile: holds a valid target
+  off = align_up(off + static_cast<size_t>(p->m_tiles) * 4);
+  p->off_active = off;  // active tiles, ascending, then their count
+  off = align_up(off + static_cast<size_t>(p->m_tiles + 1) * 4);
   p->off_dxf = off;
   if (p->v_blocks > 1) off = align_up(off + static_cast<size_t>(N) * H * 4);
   p->off_dwf = off;
@@ -388,8 +392,15 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   const long long* nv = reinterpret_cast<const long long*>(n_valid);
   int* targets = reinterpret_cast<int*>(ws + p.off_t);
   const int S = static_cast<int>(seq_len > 0 ? seq_len : N);
+  // Token tiles whose rows are all ignored have dZ = 0: they add nothing to dW
+  // and their dX rows are 0, so the backward runs on the active tiles only.
+  int* flags = reinterpret_cast<int*>(ws + p.off_flags);
+  int* active = reinterpret_cast<int*>(ws + p.off_active);
+  int* n_active = active + p.m_tiles;
+  FLCE_CUDA(cudaMemsetAsync(flags, 0, static_cast<size_t>(p.m_tiles) * 4, s));
   FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index,
-                                static_cast<int>(V), targets, nullptr, err, s));
+                                static_cast<int>(V), targets, nullptr, err, s, flags));
+  FLCE_CUDA(launch_compact_tiles(flags, p.m_tiles, active, n_active, s));
 
   float* dxf = reinterpret_cast<float*>(ws + p.off_dxf);
   float* dwf = reinterpret_cast<float*>(ws + p.off_dwf);
@@ -401,6 +412,8 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   const bool band = dW && !dw_final;  // bf16 dW over several token blocks: FP32 band
   FLCE_CUDA(cudaMemsetAsync(counters, 0, static_cast<size_t>(p.launches) * 4, s));
   if (dX && !dx_final) FLCE_CUDA(cudaMemsetAsync(dxf, 0, static_cast<size_t>(N) * H * 4, s));
+  // rows of skipped tiles are never written by the dX tiles: start from zero
+  if (dX && dx_final) FLCE_CUDA(cudaMemsetAsync(dX, 0, static_cast<size_t>(N) * H * 2, s));
 
   BwdMaps maps;
   if (!make_tmap(&maps.x_k, X, H, N, H * 2, kBK, kBM) ||
@@ -440,17 +453,19 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
     maps.dw_out = maps.dz_st[0];
   if (!ok) return FLCE_ERR_CUDA;
 
-  // dZ blocks in vocab-major order: b = vb * n_blocks + nb
+  // dZ blocks in vocab-major order: b = vb * n_blocks + nb.  Token block nb
+  // covers active tiles [nb * Nb/256, (nb + 1) * Nb/256); with tiles skipped the
+  // last blocks hold fewer tiles or none (the kernels read the active count).
   const int nblk = p.n_blocks * p.v_blocks;
+  const int tiles_per_block = static_cast<int>(p.Nb / kPairM);
   auto block = [&](int b) {
     BlockDesc d;
     const int vb = b / p.n_blocks, nb = b % p.n_blocks;
-    const int64_t row0 = int64_t{nb} * p.Nb, col0 = int64_t{vb} * p.Vb;
-    const int64_t next = std::min<int64_t>(p.Nb, N - row0);
+    const int64_t col0 = int64_t{vb} * p.Vb;
     const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
-    d.row0 = static_cast<int>(row0);
+    d.tile0 = nb * tiles_per_block;
     d.col0 = static_cast<int>(col0);
-    d.mt = static_cast<int>(cdiv(next, kPairM));
+    d.mt = std::min(tiles_per_block, p.m_tiles - d.tile0);
     d.vt = static_cast<int>(cdiv(vext, kBN));
     d.slot = b & 1;
     return d;
@@ -458,6 +473,11 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
 
   BwdArgs base;
   std::memset(&base, 0, sizeof(base));
+  base.want_dx = dX ? 1 : 0;
+  base.want_dw = want_dw ? 1 : 0;
+  base.h_tiles = p.h_tiles;
+  base.active = active;
+  base.n_active = n_active;
   base.kb_h = static_cast<int>(cdiv(H, kBK));
   base.mn3d = mn3d ? 1 : 0;
   base.N = static_cast<int>(N);
@@ -493,9 +513,10 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   for (int lp = 0; lp <= nblk; ++lp) {
     BwdArgs a = base;
     a.counter = counters + lp;
+    int tiles = 0;  // at most this many tiles (fewer when token tiles are skipped)
     if (lp < nblk) {
       a.r = block(lp);
-      a.r_tiles = a.r.mt * a.r.vt;
+      tiles += a.r.mt * a.r.vt;
     }
     int xw_vb = -1, xw_nb = -1;
     bool overlap = lp >= 1;  // directly after the previous backward launch
@@ -504,8 +525,8 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
       a.xw = block(b);
       xw_vb = b / p.n_blocks;
       xw_nb = b % p.n_blocks;
-      if (want_dw) a.w_tiles = a.xw.vt * p.h_tiles;
-      if (dX) a.x_tiles = a.xw.mt * p.h_tiles;
+      if (want_dw) tiles += a.xw.vt * p.h_tiles;
+      if (dX) tiles += a.xw.mt * p.h_tiles;
       if (band && xw_nb == 0) {
         FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.xw.vt) * kBN * H * 4, s));
         overlap = false;
@@ -513,7 +534,6 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
     }
     if (band && lp >= 2 && (lp - 2) % p.n_blocks == p.n_blocks - 1)
       overlap = false;  // a band downcast sits between this launch and the previous one
-    const int tiles = a.r_tiles + a.w_tiles + a.x_tiles;
     if (lp == 0) prof_begin(s);
     FLCE_CUDA(launch_bwd_gemm(maps, a, tiles, overlap, s));
     if (band && lp >= 1 && xw_nb == p.n_blocks - 1) {

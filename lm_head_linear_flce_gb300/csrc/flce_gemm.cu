@@ -186,17 +186,18 @@ __device__ __forceinline__ void load_dx(const CUtensorMap* tdz, const CUtensorMa
   }
 }
 // dW tile: A = dZ^T (MN-major over vocab), B = X rows of the block (MN-major over H).
-__device__ __forceinline__ void load_dw(const CUtensorMap* tdzmn, const CUtensorMap* txmn,
-                                        const CUtensorMap* tdzmn3, const CUtensorMap* txmn3,
-                                        bool mn3d, uint32_t sa, uint32_t sb, int k, int v0,
-                                        int h0, int trow0, uint32_t full, uint64_t keep) {
+// k: local dZ row of this k-block; xrow: the token row of X it corresponds to.
+__device__ __forceinline__ void load_dw(const CUtensorMap* txmn, const CUtensorMap* tdzmn3,
+                                        const CUtensorMap* txmn3, bool mn3d, uint32_t sa,
+                                        uint32_t sb, int k, int v0, int h0, int xrow,
+                                        uint32_t full, uint64_t keep) {
   tma_load_3d_pair(sa, tdzmn3, 0, k, v0 / 64, full);  // the dZ slot is always 64-aligned
   if (mn3d) {
-    tma_load_3d_pair_hint(sb, txmn3, 0, trow0 + k, h0 / 64, full, keep);
+    tma_load_3d_pair_hint(sb, txmn3, 0, xrow, h0 / 64, full, keep);
   } else {
 #pragma unroll
     for (int q = 0; q < 2; ++q)
-      tma_load_2d_pair_hint(sb + q * 8192, txmn, h0 + 64 * q, trow0 + k, full, keep);
+      tma_load_2d_pair_hint(sb + q * 8192, txmn, h0 + 64 * q, xrow, full, keep);
   }
 }
 
@@ -367,17 +368,23 @@ __device__ __forceinline__ void epi_reduce_staged(uint32_t tbase, int h0, int H,
   }
 }
 
-// Final gradient rows: bf16(scale * acc), 64 columns per chunk.
+// Final gradient rows: bf16(scale * acc), 64 columns per chunk (zeros when the
+// tile had no K, i.e. no accumulator was written).
 __device__ __forceinline__ void epi_final_staged(uint32_t tbase, int h0, int H, float scale,
                                                  Stager& st, int lane, const CUtensorMap* m,
-                                                 int y) {
+                                                 int y, bool zero = false) {
 #pragma unroll 1
   for (int c = 0; c < kBN / 64; ++c) {
     const int h = h0 + 64 * c;
     if (h >= H) break;  // warp-uniform
     float v[64];
-    tmem_ld32(tbase + 64 * c, *reinterpret_cast<float(*)[32]>(&v[0]));
-    tmem_ld32(tbase + 64 * c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+    if (zero) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = 0.f;
+    } else {
+      tmem_ld32(tbase + 64 * c, *reinterpret_cast<float(*)[32]>(&v[0]));
+      tmem_ld32(tbase + 64 * c + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
+    }
     uint32_t p[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) p[i] = pack_bf16x2(scale * v[2 * i], scale * v[2 * i + 1]);
@@ -560,21 +567,48 @@ struct Tile {
   int kind, m0, n0, k_blocks;
 };
 
+// Tiles of this launch, from the number of active token tiles (written on the
+// device before the first backward launch).
+struct Counts {
+  int mt_r, mt_xw;  // active token tiles of the R block and of the XW block
+  int r_tiles, w_tiles, x_tiles, total;
+};
+
+__device__ __forceinline__ Counts tile_counts(const BwdArgs& a) {
+  const int n = *a.n_active;
+  Counts c;
+  c.mt_r = max(0, min(a.r.mt, n - a.r.tile0));
+  c.mt_xw = max(0, min(a.xw.mt, n - a.xw.tile0));
+  c.r_tiles = c.mt_r * a.r.vt;
+  // with no active token tile a bf16 dW written directly still needs its zeros:
+  // those W tiles run with K = 0 and store 0
+  c.w_tiles = (a.want_dw && (c.mt_xw > 0 || a.dw_final)) ? a.xw.vt * a.h_tiles : 0;
+  c.x_tiles = a.want_dx ? c.mt_xw * a.h_tiles : 0;
+  c.total = c.w_tiles + c.r_tiles + c.x_tiles;
+  return c;
+}
+
+// First token row of local dZ row `l` of a block starting at active tile tile0.
+__device__ __forceinline__ int token_row(const BwdArgs& a, int tile0, int l) {
+  return a.active[tile0 + (l >> 8)] * kPairM + (l & (kPairM - 1));
+}
+
 // Ticket order: W tiles of the XW block, then R tiles of the R block, then X
 // tiles of the XW block (longest K first).  Within a kind, consecutive tickets
 // share the operand that is reused most (the H columns or the vocab rows).
-__device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, int t) {
-  if (t < a.w_tiles) {
+// m0: local row of the tile (dZ row for R/X tiles, vocab row for W tiles).
+__device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, const Counts& c, int t) {
+  if (t < c.w_tiles) {
     const int v = t % a.xw.vt, h = t / a.xw.vt;
-    return {kKindW, v * kPairM, h * kBN, a.xw.mt * (kPairM / kBK)};
+    return {kKindW, v * kPairM, h * kBN, c.mt_xw * (kPairM / kBK)};
   }
-  t -= a.w_tiles;
-  if (t < a.r_tiles) {
-    const int m = t % a.r.mt, v = t / a.r.mt;
+  t -= c.w_tiles;
+  if (t < c.r_tiles) {
+    const int m = t % c.mt_r, v = t / c.mt_r;
     return {kKindR, m * kPairM, v * kBN, a.kb_h};
   }
-  t -= a.r_tiles;
-  const int m = t % a.xw.mt, h = t / a.xw.mt;
+  t -= c.r_tiles;
+  const int m = t % c.mt_xw, h = t / c.mt_xw;
   return {kKindX, m * kPairM, h * kBN, a.xw.vt * (kBN / kBK)};
 }
 
@@ -588,7 +622,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const int lane = threadIdx.x & 31;
   const int rank = static_cast<int>(cluster_ctarank());
   const bool leader = rank == 0;
-  const int total = a.w_tiles + a.r_tiles + a.x_tiles;
+  const Counts cnt = tile_counts(a);
+  const int total = cnt.total;
   const uint32_t tmem = pair_setup(s, warp);
   const WaitCtx w{s.abort_flag, a.err, a.wait_limit_ns};
   // The next backward launch may start on SMs this grid frees.  It runs its
@@ -603,7 +638,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       bool prior_done = false;  // the preceding grid (which wrote this dZ slot) has completed
       const uint64_t keep = l2_policy_evict_last();
       const CUtensorMap* dz_k = &maps.dz_k[a.xw.slot & 1];
-      const CUtensorMap* dz_mn = &maps.dz_mn[a.xw.slot & 1];
       const CUtensorMap* dz_mn3 = &maps.dz_mn3[a.xw.slot & 1];
       const bool mn3d = a.mn3d != 0;
       for (;;) {
@@ -624,7 +658,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         }
         ring.advance<kTicketRing>();
         if (t >= total) break;
-        const Tile tile = decode_ticket(a, t);
+        const Tile tile = decode_ticket(a, cnt, t);
         if (tile.kind != kKindR && !prior_done) {
           griddep_wait();
           prior_done = true;
@@ -642,14 +676,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const int k = kb * kBK;
           if (leader) mbar_arrive_expect_tx(full, kStageTx);
           if (tile.kind == kKindR)
-            load_xw(&maps.x_k, &maps.w_k, sa, sb, k, a.r.row0 + arow, a.r.col0 + bcol, full_c,
-                    keep);
+            load_xw(&maps.x_k, &maps.w_k, sa, sb, k, token_row(a, a.r.tile0, arow),
+                    a.r.col0 + bcol, full_c, keep);
           else if (tile.kind == kKindX)
             load_dx(dz_k, &maps.w_mn, &maps.w_mn3, mn3d, sa, sb, k, arow, bcol, a.xw.col0,
                     full_c);
           else
-            load_dw(dz_mn, &maps.x_mn, dz_mn3, &maps.x_mn3, mn3d, sa, sb, k, arow, bcol,
-                    a.xw.row0, full_c, keep);
+            load_dw(&maps.x_mn, dz_mn3, &maps.x_mn3, mn3d, sa, sb, k, arow, bcol,
+                    token_row(a, a.xw.tile0, k), full_c, keep);
           issued |= 1u << pipe.idx;
           pipe.advance<kStages>();
         }
@@ -666,7 +700,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         mbar_arrive(s.qempty + 8 * ring.idx);
         ring.advance<kTicketRing>();
         if (t >= total) break;
-        const Tile tile = decode_ticket(a, t);
+        const Tile tile = decode_ticket(a, cnt, t);
         if (!wait_parity_cluster(s.tempty + 8 * accr.idx, accr.phase ^ 1u, w)) break;
         tc_fence_after();
         const uint32_t d = tmem + accr.idx * kAccCols;
@@ -701,12 +735,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (lane == 0) mbar_arrive_cluster(mapa_shared(s.qempty + 8 * ring.idx, 0));
       ring.advance<kTicketRing>();
       if (t >= total) break;
-      const Tile tile = decode_ticket(a, t);
+      const Tile tile = decode_ticket(a, cnt, t);
       // per-row context, read before waiting for the accumulator
       int tgt = -1;
       float lse2 = 0.f;
       if (tile.kind == kKindR) {
-        const int grow = a.r.row0 + tile.m0 + r;
+        const int grow = token_row(a, a.r.tile0, tile.m0 + r);
         if (grow < a.N) {
           tgt = a.targets[grow];
           lse2 = a.lse[grow] * kLog2e;
@@ -725,13 +759,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         epi_dz_staged(tbase, a.r.col0 + tile.n0, a.V, tgt, lse2, st, lane,
                       &maps.dz_st[a.r.slot & 1], tile.n0, y0);
       } else if (tile.kind == kKindX) {
+        const int row = token_row(a, a.xw.tile0, y0);
         if (a.dx_final)
-          epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dx_out, a.xw.row0 + y0);
+          epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dx_out, row);
         else
-          epi_reduce_staged(tbase, tile.n0, a.H, 1.f, st, lane, &maps.dx_out, a.xw.row0 + y0);
+          epi_reduce_staged(tbase, tile.n0, a.H, 1.f, st, lane, &maps.dx_out, row);
       } else {
         if (a.dw_final)
-          epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dw_out, a.xw.col0 + y0);
+          epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dw_out, a.xw.col0 + y0,
+                           tile.k_blocks == 0);
         else
           // an FP32 band (scaled later), or the caller's FP32 gradient (scaled here)
           epi_reduce_staged(tbase, tile.n0, a.H, a.dw_accumulate ? scale : 1.f, st, lane,

@@ -56,11 +56,14 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;
 };
 
-// One dZ block of the backward: token rows [row0, row0 + mt*256) x vocab
-// columns [col0, col0 + vt*256), stored in dZ slot `slot`.
+// One dZ block of the backward: the active 256-row token tiles
+// active[tile0 .. tile0 + mt) (at most `mt`; fewer when tiles whose rows are all
+// ignored were dropped) x vocab columns [col0, col0 + vt*256), stored in dZ
+// slot `slot`.  Local dZ row l of the block is token row
+// active[tile0 + l / 256] * 256 + l % 256.
 struct BlockDesc {
-  int row0, col0;
-  int mt;     // 256-row token tiles
+  int tile0, col0;
+  int mt;     // at most this many 256-row token tiles
   int vt;     // 256-column vocab tiles (R tiles per row tile; W tiles; X tiles' K / 256)
   int slot;
 };
@@ -90,7 +93,10 @@ struct BwdMaps {
 // One backward launch: R tiles of block `r`, W and X tiles of block `xw`.
 struct BwdArgs {
   BlockDesc r, xw;
-  int r_tiles, w_tiles, x_tiles;
+  int want_dx, want_dw;  // which contractions run (dX tiles, dW tiles)
+  int h_tiles;           // 256-column tiles of H
+  const int* active;     // active 256-row token tiles, ascending
+  const int* n_active;   // number of entries of `active`
   int kb_h;  // K blocks of the recompute (ceil(H / 64))
   int mn3d;  // 1: MN-major halves load as one 3-D box (w_mn3 / x_mn3 / dz_mn3)
   int N, H, V;
@@ -121,7 +127,8 @@ struct Plan {
   int n_blocks, v_blocks;
   bool multi_n;           // more than one token block: dW needs an FP32 band
   int launches;           // backward GEMM launches (one per dZ block, plus one)
-  size_t off_err, off_t, off_zt, off_part, off_lossp, off_cnt, off_dxf, off_dwf, off_dz;
+  size_t off_err, off_t, off_zt, off_part, off_lossp, off_cnt, off_flags, off_active, off_dxf,
+      off_dwf, off_dz;
   size_t total;
 };
 
@@ -131,9 +138,14 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p);
 void note_launch();
 
 // Launchers (return cudaGetLastError()).
+// tile_flags (or null): set to 1 for every 256-row tile holding a valid target.
 cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int shift,
                                 int64_t ignore_index, int V, int* targets,
-                                long long* n_valid, int* err, cudaStream_t st);
+                                long long* n_valid, int* err, cudaStream_t st,
+                                int* tile_flags = nullptr);
+// active[0 .. *n_active) = indices of the flagged tiles, ascending.
+cudaError_t launch_compact_tiles(const int* tile_flags, int m_tiles, int* active, int* n_active,
+                                 cudaStream_t st);
 cudaError_t launch_merge_lse(const float2* partials, int nchunks, int N, const float* zt,
                              const int* targets, float* lse, double* loss_partials,
                              cudaStream_t st, int* nblocks_out);

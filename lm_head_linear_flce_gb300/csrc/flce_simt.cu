@@ -20,7 +20,7 @@ constexpr int kFinalThreads = 256;
 __global__ void prep_targets_kernel(const int64_t* __restrict__ labels, int N, int seq_len,
                                     int shift, int64_t ignore_index, int V,
                                     int* __restrict__ targets, unsigned long long* n_valid,
-                                    int* err) {
+                                    int* err, int* tile_flags) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   int ok = 0;
   if (i < N) {
@@ -36,6 +36,7 @@ __global__ void prep_targets_kernel(const int64_t* __restrict__ labels, int N, i
       if (lab >= 0 && lab < V) {
         t = static_cast<int>(lab);
         ok = 1;
+        if (tile_flags) tile_flags[i >> 8] = 1;  // this 256-row tile has a target
       } else {
         atomicOr(err, kErrLabel);
       }
@@ -123,6 +124,30 @@ __global__ void downcast_kernel(const float4* __restrict__ src, uint4* __restric
   }
 }
 
+// Lists the flagged tiles in ascending order (one block; a block-wide scan
+// per 1024 tiles).
+__global__ void compact_tiles_kernel(const int* __restrict__ flags, int m_tiles,
+                                     int* __restrict__ active, int* __restrict__ n_active) {
+  __shared__ int scan[1024];
+  int base = 0;
+  for (int t0 = 0; t0 < m_tiles; t0 += 1024) {
+    const int t = t0 + threadIdx.x;
+    const int f = (t < m_tiles && flags[t]) ? 1 : 0;
+    scan[threadIdx.x] = f;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+      const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+      __syncthreads();
+      scan[threadIdx.x] += v;
+      __syncthreads();
+    }
+    if (f) active[base + scan[threadIdx.x] - 1] = t;
+    base += scan[1023];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *n_active = base;
+}
+
 // Waits on a barrier that nothing will ever complete; the bounded wait must
 // give up, record the timeout and let the kernel return.
 __global__ void selftest_wait_kernel(unsigned long long limit_ns, int* err) {
@@ -141,12 +166,12 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns, int* err) {
 
 cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int shift,
                                 int64_t ignore_index, int V, int* targets, long long* n_valid,
-                                int* err, cudaStream_t st) {
+                                int* err, cudaStream_t st, int* tile_flags) {
   if (N <= 0) return cudaSuccess;
   const int blocks = (N + kPrepThreads - 1) / kPrepThreads;
   prep_targets_kernel<<<blocks, kPrepThreads, 0, st>>>(
       labels, N, seq_len, shift, ignore_index, V, targets,
-      reinterpret_cast<unsigned long long*>(n_valid), err);
+      reinterpret_cast<unsigned long long*>(n_valid), err, tile_flags);
   note_launch();
   return cudaGetLastError();
 }
@@ -185,6 +210,13 @@ cudaError_t launch_downcast(const float* src, __nv_bfloat16* dst, size_t count,
   downcast_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(src),
                                           reinterpret_cast<uint4*>(dst), count8, grad_loss,
                                           n_valid, reduction);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact_tiles(const int* tile_flags, int m_tiles, int* active, int* n_active,
+                                 cudaStream_t st) {
+  compact_tiles_kernel<<<1, 1024, 0, st>>>(tile_flags, m_tiles, active, n_active);
   note_launch();
   return cudaGetLastError();
 }

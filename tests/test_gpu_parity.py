@@ -211,3 +211,24 @@ def test_default_blocking_several_token_blocks():
 def test_many_vocab_blocks_few_rows():
     X, W, labels = workloads.random_case(96, 128, 70000, seed=33, w_std=0.1)
     check_against_oracle(X, W, labels, reduction="sum")
+
+
+@pytest.mark.parametrize("blocks", [None, (256, 256 * 1024)])
+def test_fully_ignored_token_tiles_are_skipped_correctly(blocks):
+    # a long masked prompt (rows 0..1099) and a masked span (1400..1799): several
+    # 256-row tiles hold no target and are dropped from the backward
+    if blocks:
+        flce.flce_set_backward_block(*blocks)
+    N, H, V = 2300, 128, 3000
+    X, W, labels = workloads.random_case(N, H, V, seed=70, ignore_frac=0.05)
+    labels[:1100] = -100
+    labels[1400:1800] = -100
+    check_against_oracle(X, W, labels, grad=1.25)
+    got, _ = check_against_oracle(X, W, labels, seq_len=N, shift=True, reduction="sum")
+    assert not got["dX"][:1024].any()
+
+
+def test_only_last_tile_active():
+    X, W, labels = workloads.random_case(1024, 64, 900, seed=71, ignore_frac=0.0)
+    labels[:1000] = -100
+    check_against_oracle(X, W, labels)
