@@ -294,6 +294,19 @@ def run_ours(args, world, rank, local):
 
     peaks, src = load_peaks()
     flops = wl.flops
+    # The backward skips 256-row token tiles without any target; FLOPs actually
+    # executed per step (reported beside the algorithmic 8*N*H*V):
+    tgt = torch.full((N,), -100, dtype=torch.int64)
+    if wl.shift:
+        lab = Lh.view(-1, wl.S)
+        tgt.view(-1, wl.S)[:, :-1] = lab[:, 1:]
+    else:
+        tgt.copy_(Lh)
+    has = (tgt != -100).view(-1)
+    pad = (-N) % 256
+    tiles = torch.cat([has, torch.zeros(pad, dtype=torch.bool)]).view(-1, 256).any(1)
+    active_rows = min(N, int(tiles.sum()) * 256)
+    exec_flops = 2 * N * H * V + 6 * active_rows * H * V
     tflops = flops / (ms_step / 1e3) / 1e12 * 1.0
     tflops_all = world * tflops
     # dominant tensor-core kernel of the step: forward launch (2NHV) or the
@@ -334,6 +347,8 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (W is %.2f GB); no flush" % (V * H * 2 / 1e9)},
         "tflops": round(tflops_all, 1),
+        "executed_tflops": round(world * exec_flops / (ms_step / 1e3) / 1e12, 1),
+        "executed_flops_per_step": exec_flops,
         "pct_bf16_peak": round(100 * tflops / peak, 2),
         "pct_bf16_peak_basis": f"bf16_tflops_sustained {peak} ({src}), 8*N*H*V per step",
         "peak_extra_hbm_bytes": int(extra),

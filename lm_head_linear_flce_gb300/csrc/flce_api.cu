@@ -239,6 +239,8 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   off = align_up(off + static_cast<size_t>(p->v_units) * N * 8);
   p->off_lossp = off;
   off = align_up(off + static_cast<size_t>(cdiv(N, 256) + 1) * 8);
+  p->off_fcnt = off;  // forward unit ticket
+  off = align_up(off + 4);
   const size_t fwd_end = off;
   // backward view (overlaps the forward view: the workspace need not persist)
   p->launches = p->n_blocks * p->v_blocks + 1;
@@ -321,6 +323,7 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
     FLCE_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
     return FLCE_OK;
   }
+  FLCE_CUDA(cudaMemsetAsync(ws + p.off_fcnt, 0, 4, s));
   int* targets = reinterpret_cast<int*>(ws + p.off_t);
   float* zt = reinterpret_cast<float*>(ws + p.off_zt);
   float2* part = reinterpret_cast<float2*>(ws + p.off_part);
@@ -346,6 +349,7 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   a.targets = targets;
   a.partials = part;
   a.zt = zt;
+  a.counter = reinterpret_cast<int*>(ws + p.off_fcnt);
   a.err = err;
   a.wait_limit_ns = g_wait_limit_ns.load();
   FLCE_CUDA(profiled(0, s, [&] { return launch_fwd_gemm(tx, tw, a, a.units, s); }));

@@ -418,36 +418,55 @@ __device__ void drain_mma(const Smem& s, const WaitCtx& w0) {
 }
 
 // ======================================================================= FWD
-// Units are dealt round robin over the CTA pairs; a unit is `group`
-// consecutive vocab tiles of one row tile.  Units with the same vocab group are
-// adjacent so pairs running at the same time share the W rows in L2.
-struct FwdSeq {
-  int unit, g;
-  __device__ void begin() {
-    unit = blockIdx.x >> 1;
-    g = 0;
-  }
-  __device__ bool valid(const GemmArgs& a) const { return unit < a.units; }
-  __device__ int mt(const GemmArgs& a) const { return unit % a.tiles_m; }
-  __device__ int nt(const GemmArgs& a) const { return (unit / a.tiles_m) * a.group + g; }
-  __device__ bool last_in_unit(const GemmArgs& a) const {
-    return g + 1 == a.group || nt(a) + 1 >= a.tiles_n;
-  }
-  __device__ void next(const GemmArgs& a) {
-    if (last_in_unit(a)) {
-      unit += gridDim.x >> 1;
-      g = 0;
+// A work unit is `group` consecutive vocab tiles of one 256-row tile; units of
+// the same vocab group are numbered consecutively.  The loss forward hands
+// units out by a global atomic ticket (the leader's producer takes it and
+// publishes it to both CTAs' ticket rings), so pairs running at the same time
+// always work on neighbouring units and share the W rows in L2, however far
+// their progress drifts apart.  The logits path, which has no workspace for a
+// ticket counter, deals units round robin instead.
+
+// Next unit for a role.  `leader_producer` takes tickets; the other roles read
+// them from this CTA's ring.  Returns false if aborted.
+template <bool DYN>
+__device__ __forceinline__ bool next_unit(const GemmArgs& a, const Smem& s, Ring& ring,
+                                          int& unit, bool leader_producer, bool peer_producer,
+                                          bool cluster_scope, int lane, bool whole_warp,
+                                          const WaitCtx& w) {
+  if constexpr (!DYN) {
+    unit = unit < 0 ? static_cast<int>(blockIdx.x >> 1) : unit + static_cast<int>(gridDim.x >> 1);
+    return true;
+  } else {
+    if (leader_producer) {
+      unit = atomicAdd(a.counter, 1);
+      if (!wait_parity_cluster(s.qempty + 8 * ring.idx, ring.phase ^ 1u, w)) return false;
+      s.tickets_p[ring.idx] = unit;
+      st_shared_cluster_u32(mapa_shared(s.tickets + 4 * ring.idx, 1), static_cast<uint32_t>(unit));
+      mbar_arrive(s.qfull + 8 * ring.idx);
+      mbar_arrive_cluster(mapa_shared(s.qfull + 8 * ring.idx, 1));
     } else {
-      ++g;
+      const bool ok = cluster_scope ? wait_parity_cluster(s.qfull + 8 * ring.idx, ring.phase, w)
+                                    : wait_parity(s.qfull + 8 * ring.idx, ring.phase, w);
+      if (!ok) return false;
+      unit = s.tickets_p[ring.idx];
+      if (whole_warp) __syncwarp();
+      if (!whole_warp || lane == 0) {
+        if (peer_producer || cluster_scope)
+          mbar_arrive_cluster(mapa_shared(s.qempty + 8 * ring.idx, 0));
+        else
+          mbar_arrive(s.qempty + 8 * ring.idx);
+      }
     }
+    ring.advance<kTicketRing>();
+    return true;
   }
-};
+}
 
 }  // namespace
 
-// MODE kFwdLse: the forward of the loss (log-sum-exp epilogue).
+// MODE kFwdLse: the forward of the loss (log-sum-exp epilogue), dynamic units.
 // MODE kFwdLogits: plain logits Z = X W^T rounded to bf16 and stored through
-// shared-memory staging (the inference path with no labels).
+// shared-memory staging (the inference path with no labels), static units.
 constexpr int kFwdLse = 0;
 constexpr int kFwdLogits = 1;
 
@@ -456,6 +475,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     flce_fwd_kernel(const __grid_constant__ CUtensorMap tma_x,
                     const __grid_constant__ CUtensorMap tma_w,
                     const __grid_constant__ CUtensorMap tma_out, const GemmArgs a) {
+  constexpr bool kDyn = MODE == kFwdLse;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const Smem s = carve_smem(smem_raw, MODE == kFwdLogits ? 4 * 2 * kStageBufBytes : 0);
   const int warp = threadIdx.x >> 5;
@@ -471,90 +491,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      Ring pipe;
+      Ring pipe, ring;
       uint32_t issued = 0;
       const uint64_t keep = l2_policy_evict_last();
-      FwdSeq seq;
-      for (seq.begin(); seq.valid(a); seq.next(a)) {
-        const int arow = seq.mt(a) * kPairM + kBM * rank;
-        const int brow = seq.nt(a) * kBN + kHalfN * rank;
-        bool ok = true;
-        for (int kb = 0; kb < a.k_blocks && ok; ++kb) {
-          ok = wait_parity(s.empty + 8 * pipe.idx, pipe.phase ^ 1u, w);
-          if (!ok) break;
-          const uint32_t full = s.full + 8 * pipe.idx;
-          if (leader) mbar_arrive_expect_tx(full, kStageTx);
-          load_xw(&tma_x, &tma_w, s.a_base + pipe.idx * kAStageBytes,
-                  s.b_base + pipe.idx * kBStageBytes, kb * kBK, arow, brow,
-                  mapa_shared(full, 0), keep);
-          issued |= 1u << pipe.idx;
-          pipe.advance<kStages>();
+      int u = -1;
+      bool ok = true;
+      while (ok && next_unit<kDyn>(a, s, ring, u, leader, !leader, true, lane, false, w) &&
+             u < a.units) {
+        const int arow = (u % a.tiles_m) * kPairM + kBM * rank;
+        for (int g = 0; g < a.group && ok; ++g) {
+          const int nt = (u / a.tiles_m) * a.group + g;
+          if (nt >= a.tiles_n) break;
+          const int brow = nt * kBN + kHalfN * rank;
+          for (int kb = 0; kb < a.k_blocks; ++kb) {
+            ok = wait_parity(s.empty + 8 * pipe.idx, pipe.phase ^ 1u, w);
+            if (!ok) break;
+            const uint32_t full = s.full + 8 * pipe.idx;
+            if (leader) mbar_arrive_expect_tx(full, kStageTx);
+            load_xw(&tma_x, &tma_w, s.a_base + pipe.idx * kAStageBytes,
+                    s.b_base + pipe.idx * kBStageBytes, kb * kBK, arow, brow,
+                    mapa_shared(full, 0), keep);
+            issued |= 1u << pipe.idx;
+            pipe.advance<kStages>();
+          }
         }
-        if (!ok) break;
       }
       if (leader) drain_loads(s, issued, pipe, w);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
-      Ring pipe, accr;
-      FwdSeq seq;
-      for (seq.begin(); seq.valid(a); seq.next(a)) {
-        if (!wait_parity_cluster(s.tempty + 8 * accr.idx, accr.phase ^ 1u, w)) break;
-        tc_fence_after();
-        if (!mma_tile<false, false>(tmem + accr.idx * kAccCols, a.k_blocks, s, pipe, w)) break;
-        mma_commit_pair_multicast(s.tfull + 8 * accr.idx, kPairMask);
-        accr.advance<kNumAcc>();
+      Ring pipe, accr, ring;
+      int u = -1;
+      bool ok = true;
+      while (ok && next_unit<kDyn>(a, s, ring, u, false, false, false, lane, false, w) &&
+             u < a.units) {
+        for (int g = 0; g < a.group; ++g) {
+          const int nt = (u / a.tiles_m) * a.group + g;
+          if (nt >= a.tiles_n) break;
+          ok = wait_parity_cluster(s.tempty + 8 * accr.idx, accr.phase ^ 1u, w);
+          if (!ok) break;
+          tc_fence_after();
+          ok = mma_tile<false, false>(tmem + accr.idx * kAccCols, a.k_blocks, s, pipe, w);
+          if (!ok) break;
+          mma_commit_pair_multicast(s.tfull + 8 * accr.idx, kPairMask);
+          accr.advance<kNumAcc>();
+        }
       }
       drain_mma(s, w);
     }
-  } else if (MODE == kFwdLogits) {
-    const int q = warp & 3;
+  } else {
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const int r = kBM * rank + q * 32 + lane;  // row of the 256-row tile
     Stager st;
     st.buf0 = s.staging + static_cast<uint32_t>(q) * 2 * kStageBufBytes;
-    Ring accr;
-    FwdSeq seq;
-    for (seq.begin(); seq.valid(a); seq.next(a)) {
-      const int y0 = seq.mt(a) * kPairM + kBM * rank + 32 * q;  // first row of this warp
-      const int n0 = seq.nt(a) * kBN;
-      if (!wait_parity(s.tfull + 8 * accr.idx, accr.phase, w)) break;
-      tc_fence_after();
-      const uint32_t tbase =
-          tmem + (static_cast<uint32_t>(q * 32) << 16) + accr.idx * kAccCols;
-      epi_final_staged(tbase, n0, a.V, 1.f, st, lane, &tma_out, y0);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(s.tempty + 8 * accr.idx, 0));
-      accr.advance<kNumAcc>();
+    Ring accr, ring;
+    int u = -1;
+    bool ok = true;
+    while (ok && next_unit<kDyn>(a, s, ring, u, false, false, true, lane, true, w) &&
+           u < a.units) {
+      const int row = (u % a.tiles_m) * kPairM + r;
+      const int t = (MODE == kFwdLse && row < a.N) ? a.targets[row] : -1;
+      float run_m = -INFINITY, run_s = 0.f;
+      for (int g = 0; g < a.group; ++g) {
+        const int nt = (u / a.tiles_m) * a.group + g;
+        if (nt >= a.tiles_n) break;
+        ok = wait_parity(s.tfull + 8 * accr.idx, accr.phase, w);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tbase =
+            tmem + (static_cast<uint32_t>(q * 32) << 16) + accr.idx * kAccCols;
+        if (MODE == kFwdLogits)
+          epi_final_staged(tbase, nt * kBN, a.V, 1.f, st, lane, &tma_out, row - lane);
+        else
+          epi_lse(tbase, nt * kBN, a.V, t, a.zt + (row < a.N ? row : 0), run_m, run_s);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(s.tempty + 8 * accr.idx, 0));
+        accr.advance<kNumAcc>();
+      }
+      if (MODE == kFwdLse && ok && row < a.N)
+        a.partials[static_cast<size_t>(u / a.tiles_m) * a.N + row] = make_float2(run_m, run_s);
     }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
-  } else {
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = kBM * rank + q * 32 + lane;  // row of the 256-row tile
-    Ring accr;
-    float run_m = -INFINITY, run_s = 0.f;
-    FwdSeq seq;
-    for (seq.begin(); seq.valid(a); seq.next(a)) {
-      const int row = seq.mt(a) * kPairM + r;
-      const int n0 = seq.nt(a) * kBN;
-      const int t = row < a.N ? a.targets[row] : -1;
-      if (seq.g == 0) {
-        run_m = -INFINITY;
-        run_s = 0.f;
-      }
-      if (!wait_parity(s.tfull + 8 * accr.idx, accr.phase, w)) break;
-      tc_fence_after();
-      const uint32_t tbase =
-          tmem + (static_cast<uint32_t>(q * 32) << 16) + accr.idx * kAccCols;
-      epi_lse(tbase, n0, a.V, t, a.zt + (row < a.N ? row : 0), run_m, run_s);
-      tc_fence_before();
+    if (MODE == kFwdLogits) {
+      if (lane == 0) bulk_wait_all();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(s.tempty + 8 * accr.idx, 0));
-      accr.advance<kNumAcc>();
-      if (seq.last_in_unit(a) && row < a.N) {
-        const int chunk = seq.nt(a) / a.group;
-        a.partials[static_cast<size_t>(chunk) * a.N + row] = make_float2(run_m, run_s);
-      }
     }
   }
   pair_teardown(tmem, warp);

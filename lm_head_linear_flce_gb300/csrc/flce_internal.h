@@ -52,6 +52,7 @@ struct GemmArgs {
   const int* targets;  // [N], -1 = no valid target
   float2* partials;    // [units_n][N]: per-row (max, sum exp(z - max)) over a work unit
   float* zt;           // [N]: target logit
+  int* counter;        // unit ticket counter (starts at 0); loss forward only
   int* err;
   unsigned long long wait_limit_ns;
 };
@@ -127,8 +128,8 @@ struct Plan {
   int n_blocks, v_blocks;
   bool multi_n;           // more than one token block: dW needs an FP32 band
   int launches;           // backward GEMM launches (one per dZ block, plus one)
-  size_t off_err, off_t, off_zt, off_part, off_lossp, off_cnt, off_flags, off_active, off_dxf,
-      off_dwf, off_dz;
+  size_t off_err, off_t, off_zt, off_part, off_lossp, off_fcnt, off_cnt, off_flags, off_active,
+      off_dxf, off_dwf, off_dz;
   size_t total;
 };
 

@@ -125,7 +125,8 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
   const size_t off_zt = off_t + up(static_cast<size_t>(N) * 4);
   const size_t off_part = off_zt + up(static_cast<size_t>(N) * 4);
   const size_t off_lossp = off_part + up(static_cast<size_t>(v_units) * N * 8);
-  const size_t need = off_lossp + up(static_cast<size_t>((N + 255) / 256 + 1) * 8);
+  const size_t off_cnt = off_lossp + up(static_cast<size_t>((N + 255) / 256 + 1) * 8);
+  const size_t need = off_cnt + up(4);
   if (need > kNoallocScratchBytes) return FLCE_ERR_WORKSPACE_TOO_SMALL;
 
   int dev = 0;
@@ -147,6 +148,8 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     float* zt = reinterpret_cast<float*>(base + off_zt);
     float2* part = reinterpret_cast<float2*>(base + off_part);
     double* lossp = reinterpret_cast<double*>(base + off_lossp);
+    int* counter = reinterpret_cast<int*>(base + off_cnt);
+    if (cudaMemsetAsync(counter, 0, 4, s) != cudaSuccess) return FLCE_ERR_CUDA;
     const int S = static_cast<int>(seq_len > 0 ? seq_len : N);
     if (launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index,
                             static_cast<int>(V), targets, reinterpret_cast<long long*>(n_valid),
@@ -168,6 +171,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     a.targets = targets;
     a.partials = part;
     a.zt = zt;
+    a.counter = counter;
     a.err = err;
     a.wait_limit_ns = kNoallocWaitNs;
     if (launch_fwd_gemm(tx, tw, a, a.units, s) != cudaSuccess)
