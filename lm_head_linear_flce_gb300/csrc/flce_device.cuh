@@ -294,6 +294,16 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* 
       : "memory");
 }
 
+// tma_store_2d with an L2 eviction-priority hint.
+__device__ __forceinline__ void tma_store_2d_hint(const void* tmap, uint32_t src, int32_t c0,
+                                                  int32_t c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(tmap),
+      "r"(src), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
 // tma_reduce_add_2d with an L2 eviction-priority hint.
 __device__ __forceinline__ void tma_reduce_add_2d_hint(const void* tmap, uint32_t src, int32_t c0,
                                                        int32_t c1, uint64_t policy) {

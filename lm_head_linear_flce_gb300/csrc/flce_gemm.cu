@@ -615,7 +615,7 @@ __device__ __forceinline__ int token_row(const BwdArgs& a, int tile0, int l) {
 
 // Ticket order: W tiles of the XW block, then R tiles of the R block, then X
 // tiles of the XW block (longest K first).  Within a kind, consecutive tickets
-// share the operand that is reused most (the H columns or the vocab rows).
+// share an operand (the H columns, the vocab rows or the dZ rows).
 // m0: local row of the tile (dZ row for R/X tiles, vocab row for W tiles).
 __device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, const Counts& c, int t) {
   if (t < c.w_tiles) {
@@ -628,7 +628,8 @@ __device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, const Counts& c,
     return {kKindR, m * kPairM, v * kBN, a.kb_h};
   }
   t -= c.r_tiles;
-  const int m = t % c.mt_xw, h = t / c.mt_xw;
+  // dX tiles H-fastest: the pairs running at once share few dZ row blocks
+  const int h = t % a.h_tiles, m = t / a.h_tiles;
   return {kKindX, m * kPairM, h * kBN, a.xw.vt * (kBN / kBK)};
 }
 
