@@ -57,8 +57,7 @@ def library() -> ctypes.CDLL:
             f"{library_path} is missing: build it with lm_head_linear_flce_gb300._build.build() "
             "(nvcc, sm_103a); there is no fallback implementation")
     lib = ctypes.CDLL(library_path)
-    c_i64, c_sz, c_p, c_int, c_f = (ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p,
-                                    ctypes.c_int, ctypes.c_float)
+    c_i64, c_sz, c_p, c_int = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
     lib.flce_workspace_size.argtypes = [c_i64, c_i64, c_i64]
     lib.flce_workspace_size.restype = c_sz
     lib.flce_forward.argtypes = [c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i64, c_i64, c_int, c_int,

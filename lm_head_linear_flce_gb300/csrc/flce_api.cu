@@ -426,8 +426,6 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
       !make_tmap(&maps.x_mn, X, H, N, H * 2, 64, 64) ||
       !make_tmap(&maps.dz_k[0], dz0, p.Vb, p.Nb, p.dz_ld * 2, kBK, kBM) ||
       !make_tmap(&maps.dz_k[1], dz1, p.Vb, p.Nb, p.dz_ld * 2, kBK, kBM) ||
-      !make_tmap(&maps.dz_mn[0], dz0, p.Vb, p.Nb, p.dz_ld * 2, 64, 64) ||
-      !make_tmap(&maps.dz_mn[1], dz1, p.Vb, p.Nb, p.dz_ld * 2, 64, 64) ||
       !make_tmap(&maps.dz_st[0], dz0, p.Vb, p.Nb, p.dz_ld * 2, 64, 32) ||
       !make_tmap(&maps.dz_st[1], dz1, p.Vb, p.Nb, p.dz_ld * 2, 64, 32))
     return FLCE_ERR_CUDA;

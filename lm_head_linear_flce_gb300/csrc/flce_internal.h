@@ -39,7 +39,6 @@ constexpr int kBwdSmemBytes = kGemmSmemBytes + 4 * 2 * kStageBufBytes;
 
 // Kinds of GEMM tile.
 enum GemmKind : int {
-  kKindFwd = 0,  // Z = X W^T tile; epilogue: online log-sum-exp + target logit
   kKindR = 1,    // Z = X W^T tile recomputed; epilogue: dZ = softmax - onehot -> bf16 block
   kKindX = 2,    // dX tile += dZ_block . W_block; A K-major, B MN-major
   kKindW = 3,    // dW tile += dZ_block^T . X_block; A MN-major, B MN-major
@@ -76,10 +75,10 @@ struct BwdMaps {
   CUtensorMap w_mn;      // W [V][H], box 64 x 64  (X: B operand, MN-major)
   CUtensorMap x_mn;      // X [N][H], box 64 x 64  (W: B operand, MN-major)
   CUtensorMap dz_k[2];   // dZ slot [Nb][Vb], box 64 x 128 (X: A operand)
-  CUtensorMap dz_mn[2];  // dZ slot [Nb][Vb], box 64 x 64  (W: A operand, MN-major)
   // MN-major operand halves as one box each: a 3-D view (64 elements, rows,
   // 64-element groups) with box 64 x 64 rows x 2 groups lands in shared memory
-  // exactly as two 64 x 64 boxes 8 KB apart.  Used when H % 64 == 0.
+  // exactly as two 64 x 64 boxes 8 KB apart.  W and X use it when H % 64 == 0
+  // (otherwise w_mn / x_mn, two boxes); the dZ slot always does (W: A operand).
   CUtensorMap w_mn3;     // W  (64, V, H/64)
   CUtensorMap x_mn3;     // X  (64, N, H/64)
   CUtensorMap dz_mn3[2]; // dZ slot (64, Nb, Vb/64)

@@ -39,30 +39,26 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 std::mutex g_setup_mu;
 void* g_scratch_addr[kMaxDevices] = {};
-int g_sms[kMaxDevices] = {};
 
 size_t up(size_t x) { return (x + kNoallocAlign - 1) / kNoallocAlign * kNoallocAlign; }
 
-// Once per device, with that device current: device address of the scratch,
-// SM count and the compute-capability check.
-flce_status setup_device(int dev, void** scratch, int* sms) {
+// Once per device, with that device current: device address of the scratch
+// and the compute-capability check.
+flce_status setup_device(int dev, void** scratch) {
   if (dev < 0 || dev >= kMaxDevices) return FLCE_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lk(g_setup_mu);
   if (!g_scratch_addr[dev]) {
-    int major = 0, minor = 0, n = 0;
+    int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FLCE_ERR_CUDA;
     if (major != 10 || minor != 3) return FLCE_ERR_UNSUPPORTED_DEVICE;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return FLCE_ERR_CUDA;
-    g_sms[dev] = n;
     g_scratch_addr[dev] = p;
   }
   *scratch = g_scratch_addr[dev];
-  *sms = g_sms[dev];
   return FLCE_OK;
 }
 
@@ -132,8 +128,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
   void* scratch = nullptr;
-  int sms = 0;
-  flce_status st = setup_device(dev, &scratch, &sms);
+  flce_status st = setup_device(dev, &scratch);
   if (st != FLCE_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
