@@ -154,6 +154,92 @@ flce_status flce_logits(const void* X, const void* W, int64_t N, int64_t H, int6
                         void* logits, int64_t ld_logits, flce_stream_t stream);
 
 /*
+ * Vocabulary-parallel split (Megatron-LM PR #2739 "[Dev] Fix
+ * Linear-Cross-Entropy Convergence Issue": section 1, the output layer is a
+ * ColumnParallelLinear, so its vocabulary rows are split across P ranks;
+ * section 2, the d_hidden contributions of the vocabulary slices are summed in
+ * an FP32 buffer and downcast to bf16 once).  Every rank holds the same X and
+ * labels and the W rows [v_offset, v_offset + V) of a V_total-row vocabulary.
+ * Per rank, in order:
+ *
+ *   flce_forward_vocab_shard   this shard's per-row lse_r and target logit z_r
+ *   (the caller gathers every rank's lse_r and z_r, e.g. one all-gather)
+ *   flce_merge_vocab_shards    loss, the whole-vocabulary lse and n_valid
+ *   flce_backward_vocab_shard  dW of the shard; dX_acc += this shard's dX part
+ *   (the caller sums dX_acc over the ranks in FP32, e.g. one all-reduce)
+ *   flce_downcast_bf16         dX in bf16
+ *
+ * Validity is judged against the whole vocabulary: a target in [0, V_total)
+ * that lies in another rank's shard is valid here, with no one-hot term on
+ * this rank.  Labels outside [0, V_total) are reported as in flce_forward.
+ * Requires 0 <= v_offset and v_offset + V <= V_total.  The workspace is sized
+ * with flce_workspace_size(N, H, V) of the shard.
+ *
+ * flce_forward_vocab_shard
+ *   W_shard     device bf16 [V][H]: vocabulary rows v_offset .. v_offset+V-1.
+ *   lse_shard   device float [N]: log sum over this shard's columns of exp(Z_ij).
+ *   z_shard     device float [N]: Z_{i,t_i} if t_i is valid and in this shard,
+ *               else 0.
+ *   n_valid     device int64, 1 element: valid targets over the whole vocabulary.
+ */
+flce_status flce_forward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
+                                     int64_t N, int64_t H, int64_t V, int64_t v_offset,
+                                     int64_t V_total, int64_t seq_len, int64_t ignore_index,
+                                     int shift, float* lse_shard, float* z_shard,
+                                     int64_t* n_valid, void* workspace, size_t workspace_bytes,
+                                     flce_stream_t stream);
+
+/*
+ * flce_merge_vocab_shards
+ *   lse_parts, z_parts  device float [P][N]: every rank's lse_shard and z_shard,
+ *                       in any rank order (the same order in both).
+ *   labels, seq_len, ignore_index, shift   as in the shard calls; V_total the
+ *                       whole vocabulary.
+ *   loss                device float: mean or sum over valid rows of
+ *                       lse_i - z_i, with lse_i = log sum_r exp(lse_parts[r][i])
+ *                       and z_i = sum_r z_parts[r][i] (deterministic).
+ *   lse                 device float [N]: the whole-vocabulary log-sum-exp.
+ *   n_valid             device int64, 1 element.
+ *   workspace           any workspace valid for the shard calls with this N
+ *                       (it needs 256 + 4N + 8(N/256 + 2) bytes, each term
+ *                       rounded up to 256).
+ * 1 <= P <= 65536.
+ */
+flce_status flce_merge_vocab_shards(const float* lse_parts, const float* z_parts, int64_t P,
+                                    const int64_t* labels, int64_t N, int64_t V_total,
+                                    int64_t seq_len, int64_t ignore_index, int shift,
+                                    flce_reduction reduction, float* loss, float* lse,
+                                    int64_t* n_valid, void* workspace, size_t workspace_bytes,
+                                    flce_stream_t stream);
+
+/*
+ * flce_backward_vocab_shard
+ *   lse, n_valid   device, as written by flce_merge_vocab_shards.
+ *   grad_loss      device float, 1 element: g.
+ *   dX_acc         device float [N][H], 16-byte aligned, or NULL:
+ *                  dX_acc += s * dZ_r W_shard, s = g / n_valid (mean) or g
+ *                  (sum), dZ_r the shard's columns of dZ; read and written (the
+ *                  caller zeroes it first, or adds to another contribution).
+ *   dW_shard       device bf16 [V][H] or NULL: this shard's rows of dW, written.
+ * The other arguments are as in flce_forward_vocab_shard.
+ */
+flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
+                                      int64_t N, int64_t H, int64_t V, int64_t v_offset,
+                                      int64_t V_total, int64_t seq_len, int64_t ignore_index,
+                                      int shift, flce_reduction reduction, const float* lse,
+                                      const int64_t* n_valid, const float* grad_loss,
+                                      float* dX_acc, void* dW_shard, void* workspace,
+                                      size_t workspace_bytes, flce_stream_t stream);
+
+/*
+ * dst[k] = bf16(src[k]) (round to nearest even) for k < count: the one
+ * downcast of a summed FP32 gradient.  count a multiple of 8; both pointers
+ * device, 16-byte aligned.
+ */
+flce_status flce_downcast_bf16(const float* src, void* dst, int64_t count,
+                               flce_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and returns the device error word written
  * by the last flce_forward / flce_backward call that used this workspace:
  * FLCE_OK, FLCE_ERR_LABEL_OUT_OF_RANGE or FLCE_ERR_TIMEOUT (the first one

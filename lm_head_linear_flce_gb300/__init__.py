@@ -23,7 +23,8 @@ __all__ = [
     "flce_get_error", "flce_selftest_wait_timeout", "flce_set_wait_limit_ns",
     "flce_set_backward_block", "flce_kernel_launch_count", "flce_profile_enable",
     "flce_profile_collect", "PROFILE_KINDS", "flce_forward_noalloc", "flce_backward_accumulate",
-    "flce_logits",
+    "flce_logits", "flce_forward_vocab_shard", "flce_merge_vocab_shards",
+    "flce_backward_vocab_shard", "flce_downcast_bf16",
     "linear_cross_entropy", "STATUS",
 ]
 
@@ -215,6 +216,99 @@ def flce_logits(X, W):
     fn.restype = ctypes.c_int
     _check(fn(_ptr(X), _ptr(W), N, H, V, _ptr(out), ld, _stream(X.device)), "flce_logits")
     return out[:, :V] if ld != V else out
+
+
+def _fn(name, argtypes):
+    fn = getattr(library(), name)
+    fn.argtypes = argtypes
+    fn.restype = ctypes.c_int
+    return fn
+
+
+_I64, _P, _INT, _SZ = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+
+def flce_forward_vocab_shard(X, W_shard, labels, v_offset, V_total, *, seq_len=None,
+                             ignore_index=-100, shift=False, workspace=None):
+    """Calls flce_forward_vocab_shard for the vocabulary rows W_shard =
+    W[v_offset : v_offset + V]; returns (lse_shard [N] f32, z_shard [N] f32,
+    n_valid [1] i64, workspace)."""
+    _check_inputs(X, W_shard, labels)
+    N, H = X.shape
+    V = W_shard.shape[0]
+    dev = X.device
+    ws = _workspace(N, H, V, dev, workspace)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    z = torch.empty(N, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    fn = _fn("flce_forward_vocab_shard", [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+                                          _INT, _P, _P, _P, _P, _SZ, _P])
+    st = fn(_ptr(X), _ptr(W_shard), _ptr(labels), N, H, V, int(v_offset), int(V_total),
+            int(seq_len or 0), int(ignore_index), int(bool(shift)), _ptr(lse), _ptr(z),
+            _ptr(n_valid), _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "flce_forward_vocab_shard")
+    return lse, z, n_valid, ws
+
+
+def flce_merge_vocab_shards(lse_parts, z_parts, labels, V_total, *, seq_len=None,
+                            ignore_index=-100, shift=False, reduction="mean", workspace):
+    """Calls flce_merge_vocab_shards on the gathered float32 [P, N] shard
+    outputs; returns (loss [1] f32, lse [N] f32, n_valid [1] i64)."""
+    for name, t in (("lse_parts", lse_parts), ("z_parts", z_parts)):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous float32 [P, N] CUDA tensor")
+    if lse_parts.shape != z_parts.shape or labels.shape != (lse_parts.shape[1],):
+        raise ValueError("lse_parts, z_parts and labels disagree in shape")
+    P, N = lse_parts.shape
+    dev = lse_parts.device
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    fn = _fn("flce_merge_vocab_shards", [_P, _P, _I64, _P, _I64, _I64, _I64, _I64, _INT, _INT,
+                                         _P, _P, _P, _P, _SZ, _P])
+    st = fn(_ptr(lse_parts), _ptr(z_parts), P, _ptr(labels), N, int(V_total), int(seq_len or 0),
+            int(ignore_index), int(bool(shift)), _REDUCTION[reduction], _ptr(loss), _ptr(lse),
+            _ptr(n_valid), _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(st, "flce_merge_vocab_shards")
+    return loss, lse, n_valid
+
+
+def flce_backward_vocab_shard(X, W_shard, labels, v_offset, V_total, lse, n_valid, grad_loss,
+                              dX_acc=None, *, seq_len=None, ignore_index=-100, shift=False,
+                              reduction="mean", need_dW=True, workspace=None, dW=None):
+    """Calls flce_backward_vocab_shard: dX_acc (float32 [N, H] or None, modified
+    in place) += this shard's part of dX; returns (dW_shard or None, workspace)."""
+    _check_inputs(X, W_shard, labels)
+    N, H = X.shape
+    V = W_shard.shape[0]
+    if dX_acc is not None and (dX_acc.dtype != torch.float32 or tuple(dX_acc.shape) != (N, H)
+                               or not dX_acc.is_contiguous()):
+        raise ValueError("dX_acc must be a contiguous float32 [N, H] tensor")
+    dev = X.device
+    ws = _workspace(N, H, V, dev, workspace)
+    if need_dW and dW is None:
+        dW = torch.empty_like(W_shard)
+    g = grad_loss.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+    fn = _fn("flce_backward_vocab_shard", [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+                                           _INT, _INT, _P, _P, _P, _P, _P, _P, _SZ, _P])
+    st = fn(_ptr(X), _ptr(W_shard), _ptr(labels), N, H, V, int(v_offset), int(V_total),
+            int(seq_len or 0), int(ignore_index), int(bool(shift)), _REDUCTION[reduction],
+            _ptr(lse), _ptr(n_valid), _ptr(g), _ptr(dX_acc), _ptr(dW if need_dW else None),
+            _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "flce_backward_vocab_shard")
+    return (dW if need_dW else None), ws
+
+
+def flce_downcast_bf16(src, out=None):
+    """Calls flce_downcast_bf16: a bf16 copy of a float32 CUDA tensor (numel a
+    multiple of 8)."""
+    if not src.is_cuda or src.dtype != torch.float32 or not src.is_contiguous():
+        raise ValueError("src must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty(src.shape, dtype=torch.bfloat16, device=src.device)
+    fn = _fn("flce_downcast_bf16", [_P, _P, _I64, _P])
+    _check(fn(_ptr(src), _ptr(out), src.numel(), _stream(src.device)), "flce_downcast_bf16")
+    return out
 
 
 def flce_get_error(workspace) -> int:

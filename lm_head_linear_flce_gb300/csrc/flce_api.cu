@@ -19,6 +19,7 @@ namespace {
 
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;
 constexpr int64_t kMaxH = 1 << 16;
+constexpr int64_t kMaxShards = 1 << 16;
 constexpr int64_t kDefaultDzBlockElems = int64_t{32} << 20;  // bf16 dZ block: 64 MB
 constexpr int64_t kDefaultMaxBlockRows = 8192;
 constexpr size_t kAlign = 256;
@@ -303,15 +304,22 @@ void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems) {
   g_block_elems.store(max_block_elems > 0 ? max_block_elems : kDefaultDzBlockElems);
 }
 
-flce_status flce_forward(const void* X, const void* W, const int64_t* labels, int64_t N,
-                         int64_t H, int64_t V, int64_t seq_len, int64_t ignore_index, int shift,
-                         flce_reduction reduction, float* loss, float* lse, int64_t* n_valid,
-                         void* workspace, size_t workspace_bytes, flce_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of flce_forward (loss and lse over the whole vocabulary) and
+// flce_forward_vocab_shard (z_out non-null: this shard's lse and target logit).
+flce_status forward_impl(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, const VocabSlice& vs, int64_t seq_len,
+                         int64_t ignore_index, int shift, flce_reduction reduction, float* loss,
+                         float* lse, float* z_out, int64_t* n_valid, void* workspace,
+                         size_t workspace_bytes, flce_stream_t stream) {
   Plan p;
   flce_status st = check_common(X, W, labels, N, H, V, seq_len, shift, reduction, workspace,
                                 workspace_bytes, &p);
   if (st != FLCE_OK) return st;
-  if (!loss || !n_valid || (N > 0 && !lse)) return FLCE_ERR_INVALID_ARG;
+  if ((!z_out && !loss) || !n_valid || (N > 0 && !lse)) return FLCE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLCE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -320,7 +328,7 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   FLCE_CUDA(cudaMemsetAsync(err, 0, 16, s));
   FLCE_CUDA(cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s));
   if (N == 0) {
-    FLCE_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    if (loss) FLCE_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
     return FLCE_OK;
   }
   FLCE_CUDA(cudaMemsetAsync(ws + p.off_fcnt, 0, 4, s));
@@ -329,9 +337,8 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   float2* part = reinterpret_cast<float2*>(ws + p.off_part);
   double* lossp = reinterpret_cast<double*>(ws + p.off_lossp);
   const int S = static_cast<int>(seq_len > 0 ? seq_len : N);
-  FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index,
-                                static_cast<int>(V), targets,
-                                reinterpret_cast<long long*>(n_valid), err, s));
+  FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index, vs,
+                                targets, reinterpret_cast<long long*>(n_valid), err, s));
 
   CUtensorMap tx, tw;
   if (!make_tmap(&tx, X, H, N, H * 2, kBK, kBM) || !make_tmap(&tw, W, H, V, H * 2, kBK, kHalfN))
@@ -355,31 +362,31 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels, in
   FLCE_CUDA(profiled(0, s, [&] { return launch_fwd_gemm(tx, tw, a, a.units, s); }));
   int nblocks = 0;
   FLCE_CUDA(launch_merge_lse(part, p.v_units, static_cast<int>(N), zt, targets, lse, lossp, s,
-                             &nblocks));
-  FLCE_CUDA(launch_finalize_loss(lossp, nblocks, reinterpret_cast<const long long*>(n_valid),
-                                 reduction == FLCE_REDUCTION_SUM ? 1 : 0, loss, s));
+                             &nblocks, z_out));
+  if (!z_out)
+    FLCE_CUDA(launch_finalize_loss(lossp, nblocks, reinterpret_cast<const long long*>(n_valid),
+                                   reduction == FLCE_REDUCTION_SUM ? 1 : 0, loss, s));
   return FLCE_OK;
 }
 
-}  // extern "C"
-
-namespace {
-
-// Shared body of flce_backward (dW written as bf16) and
-// flce_backward_accumulate (dW_acc += scale * dZ^T X in FP32).
+// Shared body of flce_backward (dW written as bf16), flce_backward_accumulate
+// (dW_acc += scale * dZ^T X in FP32) and flce_backward_vocab_shard (dX_acc +=
+// scale * dZ W in FP32 over the shard's columns; dX is then null).
 flce_status backward_impl(const void* X, const void* W, const int64_t* labels, int64_t N,
-                          int64_t H, int64_t V, int64_t seq_len, int64_t ignore_index, int shift,
-                          flce_reduction reduction, const float* lse, const int64_t* n_valid,
-                          const float* grad_loss, void* dX, void* dW, float* dW_acc,
-                          void* workspace, size_t workspace_bytes, flce_stream_t stream) {
+                          int64_t H, int64_t V, const VocabSlice& vs, int64_t seq_len,
+                          int64_t ignore_index, int shift, flce_reduction reduction,
+                          const float* lse, const int64_t* n_valid, const float* grad_loss,
+                          void* dX, float* dX_acc, void* dW, float* dW_acc, void* workspace,
+                          size_t workspace_bytes, flce_stream_t stream) {
   Plan p;
   flce_status st = check_common(X, W, labels, N, H, V, seq_len, shift, reduction, workspace,
                                 workspace_bytes, &p);
   if (st != FLCE_OK) return st;
   if (!n_valid || !grad_loss || (N > 0 && !lse)) return FLCE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(dX) | reinterpret_cast<uintptr_t>(dW) |
-       reinterpret_cast<uintptr_t>(dW_acc)) & 15)
+       reinterpret_cast<uintptr_t>(dW_acc) | reinterpret_cast<uintptr_t>(dX_acc)) & 15)
     return FLCE_ERR_INVALID_ARG;
+  if (dX && dX_acc) return FLCE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLCE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -391,7 +398,8 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
     return FLCE_OK;  // nothing to add to dW_acc
   }
   const bool want_dw = dW || dW_acc;
-  if (!dX && !want_dw) return FLCE_OK;
+  const bool want_dx = dX || dX_acc;
+  if (!want_dx && !want_dw) return FLCE_OK;
   const int red = reduction == FLCE_REDUCTION_SUM ? 1 : 0;
   const long long* nv = reinterpret_cast<const long long*>(n_valid);
   int* targets = reinterpret_cast<int*>(ws + p.off_t);
@@ -402,16 +410,18 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   int* active = reinterpret_cast<int*>(ws + p.off_active);
   int* n_active = active + p.m_tiles;
   FLCE_CUDA(cudaMemsetAsync(flags, 0, static_cast<size_t>(p.m_tiles) * 4, s));
-  FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index,
-                                static_cast<int>(V), targets, nullptr, err, s, flags));
+  FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index, vs,
+                                targets, nullptr, err, s, flags));
   FLCE_CUDA(launch_compact_tiles(flags, p.m_tiles, active, n_active, s));
 
-  float* dxf = reinterpret_cast<float*>(ws + p.off_dxf);
+  // the caller's FP32 buffer, or the workspace accumulator when V spans
+  // several vocab blocks (a single block writes bf16 dX directly)
+  float* dxf = dX_acc ? dX_acc : reinterpret_cast<float*>(ws + p.off_dxf);
   float* dwf = reinterpret_cast<float*>(ws + p.off_dwf);
   int* counters = reinterpret_cast<int*>(ws + p.off_cnt);
   __nv_bfloat16* dz0 = reinterpret_cast<__nv_bfloat16*>(ws + p.off_dz);
   __nv_bfloat16* dz1 = dz0 + static_cast<size_t>(p.Nb) * p.dz_ld;
-  const bool dx_final = p.v_blocks == 1;
+  const bool dx_final = p.v_blocks == 1 && !dX_acc;
   const bool dw_final = !p.multi_n;
   const bool band = dW && !dw_final;  // bf16 dW over several token blocks: FP32 band
   FLCE_CUDA(cudaMemsetAsync(counters, 0, static_cast<size_t>(p.launches) * 4, s));
@@ -441,7 +451,7 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   bool ok = true;
   if (dX && dx_final)
     ok = make_tmap(&maps.dx_out, dX, H, N, H * 2, 64, 32);
-  else if (dX)
+  else if (want_dx)
     ok = make_tmap(&maps.dx_out, dxf, H, N, H * 4, 32, 32, kF32);
   else
     maps.dx_out = maps.dz_st[0];
@@ -475,7 +485,7 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
 
   BwdArgs base;
   std::memset(&base, 0, sizeof(base));
-  base.want_dx = dX ? 1 : 0;
+  base.want_dx = want_dx ? 1 : 0;
   base.want_dw = want_dw ? 1 : 0;
   base.h_tiles = p.h_tiles;
   base.active = active;
@@ -490,7 +500,10 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   base.dz[0] = dz0;
   base.dz[1] = dz1;
   base.dz_ld = static_cast<int>(p.dz_ld);
-  if (dX) {
+  if (dX_acc) {
+    base.dxf = dxf;
+    base.dx_accumulate = 1;
+  } else if (dX) {
     if (dx_final)
       base.dx_final = static_cast<__nv_bfloat16*>(dX);
     else
@@ -528,7 +541,7 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
       xw_vb = b / p.n_blocks;
       xw_nb = b % p.n_blocks;
       if (want_dw) tiles += a.xw.vt * p.h_tiles;
-      if (dX) tiles += a.xw.mt * p.h_tiles;
+      if (want_dx) tiles += a.xw.mt * p.h_tiles;
       if (band && xw_nb == 0) {
         FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.xw.vt) * kBN * H * 4, s));
         overlap = false;
@@ -552,17 +565,132 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   return FLCE_OK;
 }
 
+// A vocabulary shard: columns [v_offset, v_offset + V) of a V_total-column
+// vocabulary.
+flce_status check_slice(int64_t V, int64_t v_offset, int64_t V_total, VocabSlice* vs) {
+  if (V <= 0 || v_offset < 0 || V_total <= 0) return FLCE_ERR_INVALID_ARG;
+  if (V_total > kMaxDim) return FLCE_ERR_UNSUPPORTED_SHAPE;
+  if (v_offset > V_total - V) return FLCE_ERR_INVALID_ARG;
+  *vs = VocabSlice{V_total, v_offset, V};
+  return FLCE_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+flce_status flce_forward(const void* X, const void* W, const int64_t* labels, int64_t N,
+                         int64_t H, int64_t V, int64_t seq_len, int64_t ignore_index, int shift,
+                         flce_reduction reduction, float* loss, float* lse, int64_t* n_valid,
+                         void* workspace, size_t workspace_bytes, flce_stream_t stream) {
+  return forward_impl(X, W, labels, N, H, V, VocabSlice{V, 0, V}, seq_len, ignore_index, shift,
+                      reduction, loss, lse, nullptr, n_valid, workspace, workspace_bytes, stream);
+}
+
+flce_status flce_forward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
+                                     int64_t N, int64_t H, int64_t V, int64_t v_offset,
+                                     int64_t V_total, int64_t seq_len, int64_t ignore_index,
+                                     int shift, float* lse_shard, float* z_shard,
+                                     int64_t* n_valid, void* workspace, size_t workspace_bytes,
+                                     flce_stream_t stream) {
+  VocabSlice vs;
+  flce_status st = check_slice(V, v_offset, V_total, &vs);
+  if (st != FLCE_OK) return st;
+  if (N > 0 && !z_shard) return FLCE_ERR_INVALID_ARG;
+  // z_out must be non-null to select the shard outputs, even for N == 0
+  float dummy = 0.f;
+  return forward_impl(X, W_shard, labels, N, H, V, vs, seq_len, ignore_index, shift,
+                      FLCE_REDUCTION_MEAN, nullptr, lse_shard, z_shard ? z_shard : &dummy,
+                      n_valid, workspace, workspace_bytes, stream);
+}
+
+flce_status flce_merge_vocab_shards(const float* lse_parts, const float* z_parts, int64_t P,
+                                    const int64_t* labels, int64_t N, int64_t V_total,
+                                    int64_t seq_len, int64_t ignore_index, int shift,
+                                    flce_reduction reduction, float* loss, float* lse,
+                                    int64_t* n_valid, void* workspace, size_t workspace_bytes,
+                                    flce_stream_t stream) {
+  if (N < 0 || P <= 0 || P > kMaxShards || V_total <= 0) return FLCE_ERR_INVALID_ARG;
+  if (N > kMaxDim || V_total > kMaxDim || P * N > kMaxDim) return FLCE_ERR_UNSUPPORTED_SHAPE;
+  if (reduction != FLCE_REDUCTION_MEAN && reduction != FLCE_REDUCTION_SUM)
+    return FLCE_ERR_INVALID_ARG;
+  if (!loss || !n_valid || !workspace) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && (!lse_parts || !z_parts || !labels || !lse)) return FLCE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) return FLCE_ERR_INVALID_ARG;
+  if (shift && N > 0) {
+    const int64_t S = seq_len > 0 ? seq_len : N;
+    if (N % S != 0) return FLCE_ERR_INVALID_ARG;
+  }
+  // layout: the error word and the targets where a forward plan keeps them,
+  // then the per-block loss partials
+  const size_t off_t = align_up(16);
+  const size_t off_lossp = off_t + align_up(static_cast<size_t>(N) * 4);
+  const size_t need = off_lossp + align_up(static_cast<size_t>(cdiv(N, 256) + 1) * 8);
+  if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  flce_status st = device_info(&dev);
+  if (st != FLCE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+  FLCE_CUDA(cudaMemsetAsync(err, 0, 16, s));
+  FLCE_CUDA(cudaMemsetAsync(n_valid, 0, sizeof(int64_t), s));
+  if (N == 0) {
+    FLCE_CUDA(cudaMemsetAsync(loss, 0, sizeof(float), s));
+    return FLCE_OK;
+  }
+  int* targets = reinterpret_cast<int*>(ws + off_t);
+  double* lossp = reinterpret_cast<double*>(ws + off_lossp);
+  const int S = static_cast<int>(seq_len > 0 ? seq_len : N);
+  FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index,
+                                VocabSlice{V_total, 0, V_total}, targets,
+                                reinterpret_cast<long long*>(n_valid), err, s));
+  int nblocks = 0;
+  FLCE_CUDA(launch_merge_shards(lse_parts, z_parts, static_cast<int>(P), static_cast<int>(N),
+                                targets, lse, lossp, s, &nblocks));
+  FLCE_CUDA(launch_finalize_loss(lossp, nblocks, reinterpret_cast<const long long*>(n_valid),
+                                 reduction == FLCE_REDUCTION_SUM ? 1 : 0, loss, s));
+  return FLCE_OK;
+}
+
+flce_status flce_backward_vocab_shard(const void* X, const void* W_shard, const int64_t* labels,
+                                      int64_t N, int64_t H, int64_t V, int64_t v_offset,
+                                      int64_t V_total, int64_t seq_len, int64_t ignore_index,
+                                      int shift, flce_reduction reduction, const float* lse,
+                                      const int64_t* n_valid, const float* grad_loss,
+                                      float* dX_acc, void* dW_shard, void* workspace,
+                                      size_t workspace_bytes, flce_stream_t stream) {
+  VocabSlice vs;
+  flce_status st = check_slice(V, v_offset, V_total, &vs);
+  if (st != FLCE_OK) return st;
+  return backward_impl(X, W_shard, labels, N, H, V, vs, seq_len, ignore_index, shift, reduction,
+                       lse, n_valid, grad_loss, nullptr, dX_acc, dW_shard, nullptr, workspace,
+                       workspace_bytes, stream);
+}
+
+flce_status flce_downcast_bf16(const float* src, void* dst, int64_t count,
+                               flce_stream_t stream) {
+  if (count < 0 || count % 8 != 0) return FLCE_ERR_INVALID_ARG;
+  if (count == 0) return FLCE_OK;
+  if (!src || !dst) return FLCE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15)
+    return FLCE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  flce_status st = device_info(&dev);
+  if (st != FLCE_OK) return st;
+  FLCE_CUDA(launch_downcast(src, static_cast<__nv_bfloat16*>(dst), static_cast<size_t>(count),
+                            nullptr, nullptr, 0, reinterpret_cast<cudaStream_t>(stream)));
+  return FLCE_OK;
+}
 
 flce_status flce_backward(const void* X, const void* W, const int64_t* labels, int64_t N,
                           int64_t H, int64_t V, int64_t seq_len, int64_t ignore_index, int shift,
                           flce_reduction reduction, const float* lse, const int64_t* n_valid,
                           const float* grad_loss, void* dX, void* dW, void* workspace,
                           size_t workspace_bytes, flce_stream_t stream) {
-  return backward_impl(X, W, labels, N, H, V, seq_len, ignore_index, shift, reduction, lse,
-                       n_valid, grad_loss, dX, dW, nullptr, workspace, workspace_bytes, stream);
+  return backward_impl(X, W, labels, N, H, V, VocabSlice{V, 0, V}, seq_len, ignore_index, shift,
+                       reduction, lse, n_valid, grad_loss, dX, nullptr, dW, nullptr, workspace,
+                       workspace_bytes, stream);
 }
 
 flce_status flce_backward_accumulate(const void* X, const void* W, const int64_t* labels,
@@ -573,9 +701,9 @@ flce_status flce_backward_accumulate(const void* X, const void* W, const int64_t
                                      void* workspace, size_t workspace_bytes,
                                      flce_stream_t stream) {
   if (!dW_acc) return FLCE_ERR_INVALID_ARG;
-  return backward_impl(X, W, labels, N, H, V, seq_len, ignore_index, shift, reduction, lse,
-                       n_valid, grad_loss, dX, nullptr, dW_acc, workspace, workspace_bytes,
-                       stream);
+  return backward_impl(X, W, labels, N, H, V, VocabSlice{V, 0, V}, seq_len, ignore_index, shift,
+                       reduction, lse, n_valid, grad_loss, dX, nullptr, nullptr, dW_acc,
+                       workspace, workspace_bytes, stream);
 }
 
 flce_status flce_logits(const void* X, const void* W, int64_t N, int64_t H, int64_t V,

@@ -742,7 +742,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     const int r = kBM * rank + q * 32 + lane;  // row of the 256-row tile
     // scale g / n_valid (mean) or g (sum), applied when a tile writes bf16 directly
-    const float scale = (a.dx_final || a.dw_final || a.dw_accumulate)
+    const float scale = (a.dx_final || a.dw_final || a.dw_accumulate || a.dx_accumulate)
                             ? grad_scale(a.grad_loss, a.n_valid, a.reduction)
                             : 1.f;
     Stager st;
@@ -784,7 +784,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         if (a.dx_final)
           epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dx_out, row);
         else
-          epi_reduce_staged(tbase, tile.n0, a.H, 1.f, st, lane, &maps.dx_out, row);
+          // the FP32 accumulator (scaled at the downcast), or the caller's FP32
+          // buffer (scaled here)
+          epi_reduce_staged(tbase, tile.n0, a.H, a.dx_accumulate ? scale : 1.f, st, lane,
+                            &maps.dx_out, row);
       } else {
         if (a.dw_final)
           epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dw_out, a.xw.col0 + y0,

@@ -12,6 +12,9 @@ namespace flce {
 // Bits of the device error word (first int of the workspace).
 constexpr int kErrLabel = 1;    // a target outside [0, V) that is not ignore_index
 constexpr int kErrTimeout = 2;  // a bounded wait ran out
+// Stored target of a valid row whose label lies in another vocabulary shard:
+// no column of this call matches it, so the row has softmax terms only.
+constexpr int kTargetElsewhere = 0x7fffffff;
 
 // GEMM tile geometry (all tensor-core kernels).  Tiles are computed by a pair
 // of CTAs (a 2-CTA cluster on two SMs) with tcgen05 cta_group::2: a tile is
@@ -109,6 +112,7 @@ struct BwdArgs {
   float* dwf;                  // FP32 dW band [Vb][H], or null
   __nv_bfloat16* dw_final;     // bf16 dW written directly (single token block), or null
   int dw_accumulate;           // 1: W tiles add scale * dW into the caller's FP32 gradient
+  int dx_accumulate;           // 1: X tiles add scale * dX into the caller's FP32 buffer (dxf)
   const float* grad_loss;
   const long long* n_valid;
   int reduction;               // 0 mean, 1 sum
@@ -137,18 +141,30 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p);
 // Counts one kernel launch (see flce_kernel_launch_count).
 void note_launch();
 
+// The vocabulary columns a call holds: [v_offset, v_offset + V_local) of a
+// V_total-column vocabulary (the whole of it outside the vocabulary-parallel
+// entry points).
+struct VocabSlice {
+  int64_t V_total, v_offset, V_local;
+};
+
 // Launchers (return cudaGetLastError()).
+// targets[i]: -1 (no valid target), the local column, or kTargetElsewhere.
 // tile_flags (or null): set to 1 for every 256-row tile holding a valid target.
 cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int shift,
-                                int64_t ignore_index, int V, int* targets,
+                                int64_t ignore_index, const VocabSlice& vs, int* targets,
                                 long long* n_valid, int* err, cudaStream_t st,
                                 int* tile_flags = nullptr);
 // active[0 .. *n_active) = indices of the flagged tiles, ascending.
 cudaError_t launch_compact_tiles(const int* tile_flags, int m_tiles, int* active, int* n_active,
                                  cudaStream_t st);
+// z_out non-null: a vocabulary shard's (lse, target logit) instead of a loss.
 cudaError_t launch_merge_lse(const float2* partials, int nchunks, int N, const float* zt,
                              const int* targets, float* lse, double* loss_partials,
-                             cudaStream_t st, int* nblocks_out);
+                             cudaStream_t st, int* nblocks_out, float* z_out = nullptr);
+cudaError_t launch_merge_shards(const float* lse_parts, const float* z_parts, int P, int N,
+                                const int* targets, float* lse, double* loss_partials,
+                                cudaStream_t st, int* nblocks_out);
 cudaError_t launch_finalize_loss(const double* loss_partials, int nblocks,
                                  const long long* n_valid, int reduction, float* loss,
                                  cudaStream_t st);

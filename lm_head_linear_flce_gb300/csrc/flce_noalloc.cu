@@ -147,7 +147,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     if (cudaMemsetAsync(counter, 0, 4, s) != cudaSuccess) return FLCE_ERR_CUDA;
     const int S = static_cast<int>(seq_len > 0 ? seq_len : N);
     if (launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index,
-                            static_cast<int>(V), targets, reinterpret_cast<long long*>(n_valid),
+                            VocabSlice{V, 0, V}, targets, reinterpret_cast<long long*>(n_valid),
                             err, s) != cudaSuccess)
       return FLCE_ERR_CUDA;
     CUtensorMap tx, tw;

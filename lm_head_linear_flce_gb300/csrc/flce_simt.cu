@@ -16,9 +16,13 @@ constexpr int kFinalThreads = 256;
 // call `linear_cross_entropy(..., ignore_index=-100, shift=True, ...)` with
 // labels = input_ids in the Qwen3.5-35B-A3B LoRA SFT blog post, listings
 // `_patch_model_with_cce` and `prepare_dataset`): -1 when the row has no valid
-// target.  Counts valid rows exactly.
+// target.  Validity is judged against the whole vocabulary [0, V_total); the
+// stored target is local to the columns [v_offset, v_offset + V_local) this
+// call holds, or kTargetElsewhere when it lies in another vocabulary shard.
+// Counts valid rows exactly.
 __global__ void prep_targets_kernel(const int64_t* __restrict__ labels, int N, int seq_len,
-                                    int shift, int64_t ignore_index, int V,
+                                    int shift, int64_t ignore_index, int64_t V_total,
+                                    int64_t v_offset, int64_t V_local,
                                     int* __restrict__ targets, unsigned long long* n_valid,
                                     int* err, int* tile_flags) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -33,8 +37,9 @@ __global__ void prep_targets_kernel(const int64_t* __restrict__ labels, int N, i
     }
     int t = -1;
     if (lab != ignore_index) {
-      if (lab >= 0 && lab < V) {
-        t = static_cast<int>(lab);
+      if (lab >= 0 && lab < V_total) {
+        const int64_t loc = lab - v_offset;
+        t = (loc >= 0 && loc < V_local) ? static_cast<int>(loc) : kTargetElsewhere;
         ok = 1;
         if (tile_flags) tile_flags[i >> 8] = 1;  // this 256-row tile has a target
       } else {
@@ -47,12 +52,28 @@ __global__ void prep_targets_kernel(const int64_t* __restrict__ labels, int N, i
   if (n_valid && threadIdx.x == 0 && cnt) atomicAdd(n_valid, static_cast<unsigned long long>(cnt));
 }
 
+// Block sum of the rows' losses in a fixed tree order (FP64), written by
+// thread 0 to loss_partials[blockIdx.x].
+__device__ __forceinline__ void block_loss_sum(double row_loss, double* red,
+                                               double* __restrict__ loss_partials) {
+  red[threadIdx.x] = row_loss;
+  __syncthreads();
+  for (int s = kMergeThreads / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) loss_partials[blockIdx.x] = red[0];
+}
+
 // lse_i = M + log sum_k s_k exp(m_k - M) over the forward's per-unit partials
 // (m_k, s_k); row loss = lse_i - z_{i,t_i} for valid rows.  Each block writes
-// the sum of its rows' losses (fixed tree order, FP64).
+// the sum of its rows' losses.  With z_out (a vocabulary shard), lse is this
+// shard's log-sum-exp, z_out its target logit (0 where the target lies in
+// another shard) and no loss is formed.
 __global__ void merge_lse_kernel(const float2* __restrict__ partials, int nchunks, int N,
                                  const float* __restrict__ zt, const int* __restrict__ targets,
-                                 float* __restrict__ lse, double* __restrict__ loss_partials) {
+                                 float* __restrict__ lse, double* __restrict__ loss_partials,
+                                 float* __restrict__ z_out) {
   __shared__ double red[kMergeThreads];
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   double row_loss = 0.0;
@@ -66,15 +87,38 @@ __global__ void merge_lse_kernel(const float2* __restrict__ partials, int nchunk
     }
     const float l = M + logf(S);
     lse[i] = l;
-    if (targets[i] >= 0) row_loss = static_cast<double>(l) - static_cast<double>(zt[i]);
+    const int t = targets[i];
+    const bool here = t >= 0 && t != kTargetElsewhere;
+    if (z_out) z_out[i] = here ? zt[i] : 0.f;
+    else if (here) row_loss = static_cast<double>(l) - static_cast<double>(zt[i]);
   }
-  red[threadIdx.x] = row_loss;
-  __syncthreads();
-  for (int s = kMergeThreads / 2; s > 0; s >>= 1) {
-    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
-    __syncthreads();
+  if (!z_out) block_loss_sum(row_loss, red, loss_partials);
+}
+
+// Merge of P vocabulary shards (Megatron-LM PR #2739, section 1: the vocabulary
+// rows of the output layer are split across ranks): lse_i = log sum_r
+// exp(lse_r,i) and z_i = sum_r z_r,i (one shard holds a valid target, the
+// others give 0); row loss = lse_i - z_i for valid rows.
+__global__ void merge_shards_kernel(const float* __restrict__ lse_parts,
+                                    const float* __restrict__ z_parts, int P, int N,
+                                    const int* __restrict__ targets, float* __restrict__ lse,
+                                    double* __restrict__ loss_partials) {
+  __shared__ double red[kMergeThreads];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  double row_loss = 0.0;
+  if (i < N) {
+    float M = -INFINITY;
+    for (int r = 0; r < P; ++r) M = fmaxf(M, lse_parts[static_cast<size_t>(r) * N + i]);
+    float S = 0.f, z = 0.f;
+    for (int r = 0; r < P; ++r) {
+      S += expf(lse_parts[static_cast<size_t>(r) * N + i] - M);
+      z += z_parts[static_cast<size_t>(r) * N + i];
+    }
+    const float l = M + logf(S);
+    lse[i] = l;
+    if (targets[i] >= 0) row_loss = static_cast<double>(l) - static_cast<double>(z);
   }
-  if (threadIdx.x == 0) loss_partials[blockIdx.x] = red[0];
+  block_loss_sum(row_loss, red, loss_partials);
 }
 
 // Sum of the block partials in a fixed order; mean divides by n_valid
@@ -101,14 +145,15 @@ __global__ void finalize_loss_kernel(const double* __restrict__ loss_partials, i
   }
 }
 
-// dst = bf16_rn(scale * src), scale = g / n_valid (mean) or g (sum): the FP32
-// buffer is rounded to bf16 once, after accumulation (Megatron-LM PR #2739,
-// section 2).  Eight elements per thread; count is a multiple of 8.
+// dst = bf16_rn(scale * src), scale = g / n_valid (mean) or g (sum), or 1
+// without grad_loss: the FP32 buffer is rounded to bf16 once, after
+// accumulation (Megatron-LM PR #2739, section 2).  Eight elements per thread;
+// count is a multiple of 8.
 __global__ void downcast_kernel(const float4* __restrict__ src, uint4* __restrict__ dst,
                                 size_t count8, const float* __restrict__ grad_loss,
                                 const long long* __restrict__ n_valid, int reduction) {
-  float scale = *grad_loss;
-  if (reduction == 0) {
+  float scale = grad_loss ? *grad_loss : 1.f;
+  if (grad_loss && reduction == 0) {
     const long long n = *n_valid;
     scale = n > 0 ? scale / static_cast<float>(n) : 0.f;
   }
@@ -165,12 +210,12 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns, int* err) {
 }  // namespace
 
 cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int shift,
-                                int64_t ignore_index, int V, int* targets, long long* n_valid,
-                                int* err, cudaStream_t st, int* tile_flags) {
+                                int64_t ignore_index, const VocabSlice& vs, int* targets,
+                                long long* n_valid, int* err, cudaStream_t st, int* tile_flags) {
   if (N <= 0) return cudaSuccess;
   const int blocks = (N + kPrepThreads - 1) / kPrepThreads;
   prep_targets_kernel<<<blocks, kPrepThreads, 0, st>>>(
-      labels, N, seq_len, shift, ignore_index, V, targets,
+      labels, N, seq_len, shift, ignore_index, vs.V_total, vs.v_offset, vs.V_local, targets,
       reinterpret_cast<unsigned long long*>(n_valid), err, tile_flags);
   note_launch();
   return cudaGetLastError();
@@ -178,12 +223,24 @@ cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int s
 
 cudaError_t launch_merge_lse(const float2* partials, int nchunks, int N, const float* zt,
                              const int* targets, float* lse, double* loss_partials,
-                             cudaStream_t st, int* nblocks_out) {
+                             cudaStream_t st, int* nblocks_out, float* z_out) {
   const int blocks = (N + kMergeThreads - 1) / kMergeThreads;
   *nblocks_out = blocks;
   if (blocks == 0) return cudaSuccess;
   merge_lse_kernel<<<blocks, kMergeThreads, 0, st>>>(partials, nchunks, N, zt, targets, lse,
-                                                     loss_partials);
+                                                     loss_partials, z_out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_shards(const float* lse_parts, const float* z_parts, int P, int N,
+                                const int* targets, float* lse, double* loss_partials,
+                                cudaStream_t st, int* nblocks_out) {
+  const int blocks = (N + kMergeThreads - 1) / kMergeThreads;
+  *nblocks_out = blocks;
+  if (blocks == 0) return cudaSuccess;
+  merge_shards_kernel<<<blocks, kMergeThreads, 0, st>>>(lse_parts, z_parts, P, N, targets, lse,
+                                                        loss_partials);
   note_launch();
   return cudaGetLastError();
 }

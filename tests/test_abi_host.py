@@ -102,3 +102,47 @@ def test_plan_blocks_follow_the_tuning_knob(lib):
         lib.flce_set_backward_block(0, 0)
     assert lib.flce_workspace_size(4096, 1024, 50000) == a
     assert b != a
+
+
+def test_vocab_shard_entry_points_reject_bad_arguments_on_host(lib):
+    N, H, V, Vt = 64, 64, 100, 300
+    ws_need = lib.flce_workspace_size(N, H, V)
+    i64, c_int = ctypes.c_int64, ctypes.c_int
+
+    def fwd(v_offset=100, V_total=Vt, Vs=V, z=_fake(), wsb=ws_need):
+        return lib.flce_forward_vocab_shard(_fake(), _fake(), _fake(), i64(N), i64(H), i64(Vs),
+                                            i64(v_offset), i64(V_total), i64(0), i64(-100),
+                                            c_int(0), _fake(), z, _fake(), _fake(0x100000),
+                                            ctypes.c_size_t(wsb), None)
+
+    assert fwd(v_offset=-1) == 1
+    assert fwd(v_offset=201) == 1                 # shard runs past the vocabulary
+    assert fwd(V_total=0) == 1
+    assert fwd(z=None) == 1
+    assert fwd(wsb=ws_need - 1) == 3
+
+    def bwd(v_offset=0, V_total=Vt, dx=_fake(0x200000), dw=_fake(0x300000)):
+        return lib.flce_backward_vocab_shard(_fake(), _fake(), _fake(), i64(N), i64(H), i64(V),
+                                             i64(v_offset), i64(V_total), i64(0), i64(-100),
+                                             c_int(0), c_int(0), _fake(), _fake(), _fake(), dx,
+                                             dw, _fake(0x100000), ctypes.c_size_t(ws_need), None)
+
+    assert bwd(v_offset=250) == 1
+    assert bwd(dx=_fake(0x200004)) == 1          # FP32 buffer not 16-byte aligned
+
+    def merge(P=2, red=0, wsb=1 << 20, ws=_fake(0x100000)):
+        return lib.flce_merge_vocab_shards(_fake(), _fake(), i64(P), _fake(), i64(N), i64(Vt),
+                                           i64(0), i64(-100), c_int(0), c_int(red), _fake(),
+                                           _fake(), _fake(), ws, ctypes.c_size_t(wsb), None)
+
+    assert merge(P=0) == 1
+    assert merge(red=3) == 1
+    assert merge(wsb=256) == 3
+    assert merge(ws=_fake(0x100008)) == 1
+
+    def down(count=64, src=_fake(0x200000)):
+        return lib.flce_downcast_bf16(src, _fake(0x300000), i64(count), None)
+
+    assert down(count=12) == 1
+    assert down(count=0) == 0
+    assert down(src=_fake(0x200008)) == 1
