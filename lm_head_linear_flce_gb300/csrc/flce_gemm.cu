@@ -18,9 +18,11 @@
 // this halves the B operand traffic of a 128 x 256 single-CTA tile.
 //
 // Two kernels share the building blocks below:
-//   flce_fwd_kernel  forward; static round-robin over work units of 4 vocab
-//                    tiles of one row tile, so the epilogue can merge the
-//                    log-sum-exp of 1024 columns before writing a partial.
+//   flce_fwd_kernel  forward; work units of 4 vocab tiles of one row tile
+//                    (so the epilogue merges the log-sum-exp of 1024 columns
+//                    before writing a partial), handed out by a global ticket
+//                    that the leader's producer writes into both CTAs' rings;
+//                    the logits-only variant deals units round robin.
 //   flce_bwd_kernel  backward; one launch holds the R tiles of dZ block p and
 //                    the W and X tiles of block p-1 (two dZ slots, so the
 //                    tiles of one launch never depend on each other).  Tiles
@@ -613,21 +615,23 @@ __device__ __forceinline__ int token_row(const BwdArgs& a, int tile0, int l) {
   return a.active[tile0 + (l >> 8)] * kPairM + (l & (kPairM - 1));
 }
 
-// Ticket order: W tiles of the XW block, then R tiles of the R block, then X
-// tiles of the XW block (longest K first).  Within a kind, consecutive tickets
-// share an operand (the H columns, the vocab rows or the dZ rows).
+// Ticket order: R tiles of the R block, then W tiles of the XW block, then X
+// tiles of the XW block.  R tiles come first because only their mainloops may
+// run while the previous launch drains (the other kinds read the dZ slot it
+// writes); the launch ends on the shorter X tiles.  Within a kind, consecutive
+// tickets share an operand (the token rows, the H columns or the dZ rows).
 // m0: local row of the tile (dZ row for R/X tiles, vocab row for W tiles).
 __device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, const Counts& c, int t) {
-  if (t < c.w_tiles) {
-    const int v = t % a.xw.vt, h = t / a.xw.vt;
-    return {kKindW, v * kPairM, h * kBN, c.mt_xw * (kPairM / kBK)};
-  }
-  t -= c.w_tiles;
   if (t < c.r_tiles) {
     const int m = t % c.mt_r, v = t / c.mt_r;
     return {kKindR, m * kPairM, v * kBN, a.kb_h};
   }
   t -= c.r_tiles;
+  if (t < c.w_tiles) {
+    const int v = t % a.xw.vt, h = t / a.xw.vt;
+    return {kKindW, v * kPairM, h * kBN, c.mt_xw * (kPairM / kBK)};
+  }
+  t -= c.w_tiles;
   // dX tiles H-fastest: the pairs running at once share few dZ row blocks
   const int h = t % a.h_tiles, m = t / a.h_tiles;
   return {kKindX, m * kPairM, h * kBN, a.xw.vt * (kBN / kBK)};
