@@ -26,9 +26,9 @@
 //   flce_bwd_kernel  backward; one launch holds the R tiles of dZ block p and
 //                    the W and X tiles of block p-1 (two dZ slots, so the
 //                    tiles of one launch never depend on each other).  Tiles
-//                    are handed out by a global atomic ticket, longest first
-//                    (W, then R, then X); the leader's producer takes each
-//                    ticket and writes it into both CTAs' ticket rings.
+//                    are handed out by a global atomic ticket in the order R,
+//                    W, X (see decode_ticket); the leader's producer takes
+//                    each ticket and writes it into both CTAs' ticket rings.
 //
 // CTA layout (192 threads, one CTA per SM, persistent):
 //   warp 0      TMA producer: 6-stage ring of (A 128x64, B 128x64) bf16 halves,
