@@ -116,9 +116,11 @@ def aggregate_throughput(tokens_per_step: int, steps: int, elapsed_ms_local: flo
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock, power and throttle reasons, kept only
+    while the timed region runs (each sample carries nvidia-smi's timestamp;
+    `window(t0, t1)` gives the host-clock bounds of the region)."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
@@ -126,15 +128,27 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "-i", str(self.gpu),
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+
+    def window(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
+
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -145,23 +159,34 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
+        rows = []
         for line in out.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                rows.append((self._when(parts[0]), float(parts[1]), float(parts[2]),
+                             float(parts[3]), parts[4:8]))
             except ValueError:
                 continue
-            for name, v in zip(self.NAMES, parts[3:7]):
+        if self.t0 is not None:
+            inside = [r for r in rows if r[0] is not None and self.t0 <= r[0] <= self.t1]
+            if not inside:  # a region shorter than the sampling period: nearest samples
+                inside = [r for r in rows
+                          if r[0] is not None and self.t0 - 0.1 <= r[0] <= self.t1 + 0.1]
+            rows = inside
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for name, v in zip(self.NAMES, r[4]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(r[1] for r in rows),
+                "sm_min_mhz": min(r[1] for r in rows),
+                "sm_max_mhz": max(r[2] for r in rows),
+                "power_w": round(statistics.median(r[3] for r in rows), 1),
+                "reasons": sorted(reasons), "samples": len(rows)}
 
 
 # ---------------------------------------------------------------- our arm
@@ -219,11 +244,13 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the timed region
+    h0 = time.time()
     t0.record(stream)
     for _ in range(args.steps):
         step()
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks.window(h0, time.time())
     barrier(world)
     clk = clocks.stop()
     launches = flce.flce_kernel_launch_count() - n0
