@@ -618,17 +618,19 @@ __device__ __forceinline__ int token_row(const BwdArgs& a, int tile0, int l) {
 // Ticket order: R tiles of the R block, then W tiles of the XW block, then X
 // tiles of the XW block.  R tiles come first because only their mainloops may
 // run while the previous launch drains (the other kinds read the dZ slot it
-// writes); the launch ends on the shorter X tiles.  Within a kind, consecutive
-// tickets share an operand (the token rows, the H columns or the dZ rows).
+// writes); the launch ends on the shorter X tiles.  Within a kind the pairs
+// running at once share the larger operand: R tiles vocab-fastest (they share
+// X rows, 59 MB in all, and sweep the 29 MB W block), W tiles H-fastest (they
+// share dZ columns), X tiles H-fastest (they share dZ rows).
 // m0: local row of the tile (dZ row for R/X tiles, vocab row for W tiles).
 __device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, const Counts& c, int t) {
   if (t < c.r_tiles) {
-    const int m = t % c.mt_r, v = t / c.mt_r;
+    const int v = t % a.r.vt, m = t / a.r.vt;
     return {kKindR, m * kPairM, v * kBN, a.kb_h};
   }
   t -= c.r_tiles;
   if (t < c.w_tiles) {
-    const int v = t % a.xw.vt, h = t / a.xw.vt;
+    const int h = t % a.h_tiles, v = t / a.h_tiles;
     return {kKindW, v * kPairM, h * kBN, c.mt_xw * (kPairM / kBK)};
   }
   t -= c.w_tiles;
