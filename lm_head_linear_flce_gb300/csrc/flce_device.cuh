@@ -38,10 +38,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -264,13 +260,6 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* 
       : "memory");
 }
 
-// Brings a 2-D tile into L2 (no shared-memory destination, no completion).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
 // L2 eviction-priority policies for the cache-hinted copies below.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
@@ -294,16 +283,6 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* 
       : "memory");
 }
 
-// tma_store_2d with an L2 eviction-priority hint.
-__device__ __forceinline__ void tma_store_2d_hint(const void* tmap, uint32_t src, int32_t c0,
-                                                  int32_t c1, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
-      " [%0, {%2, %3}], [%1], %4;" ::"l"(tmap),
-      "r"(src), "r"(c0), "r"(c1), "l"(policy)
-      : "memory");
-}
-
 // tma_reduce_add_2d with an L2 eviction-priority hint.
 __device__ __forceinline__ void tma_reduce_add_2d_hint(const void* tmap, uint32_t src, int32_t c0,
                                                        int32_t c1, uint64_t policy) {
@@ -315,20 +294,6 @@ __device__ __forceinline__ void tma_reduce_add_2d_hint(const void* tmap, uint32_
 }
 
 // ---------------------------------------------------------------- tcgen05
-// Allocate `ncols` TMEM columns (power of two >= 32); the whole warp executes
-// this and the base address is written to shared memory at `dst`.
-__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -336,27 +301,10 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T for one 128 x N x 16 bf16 step, FP32 accumulate.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation issued so far by this
-// thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// ---- CTA-pair forms (cta_group::2): one warp of each CTA of the pair executes
-// alloc / relinquish / dealloc together; the even CTA issues the MMAs.
+// CTA-pair forms (cta_group::2): one warp of each CTA of the pair executes
+// alloc / relinquish / dealloc together (`ncols`: a power of two >= 32, the
+// base address written to shared memory at `dst`); the even CTA issues the
+// MMAs.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
                "r"(ncols)
@@ -392,6 +340,8 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t
       : "memory");
 }
 
+// Arrive once on `bar` (this CTA's) when all tcgen05 operations issued so far
+// by this thread have completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
