@@ -232,3 +232,15 @@ def test_only_last_tile_active():
     X, W, labels = workloads.random_case(1024, 64, 900, seed=71, ignore_frac=0.0)
     labels[:1000] = -100
     check_against_oracle(X, W, labels)
+
+
+@pytest.mark.parametrize("N,H,V", [
+    (200, 16384, 600),     # long K for the recompute and for the dX / dW tiles' H sweep
+    (64, 65536, 300),      # the largest supported H
+    (40, 64, 300001),      # a vocabulary of 300K (many vocab blocks and forward units)
+    (20000, 32, 700),      # three token blocks at the default blocking, ragged last block
+])
+def test_large_extents(N, H, V):
+    X, W, labels = workloads.random_case(N, H, V, seed=N % 97 + H % 89 + V % 83,
+                                         w_std=0.5 / np.sqrt(H) * 8)
+    check_against_oracle(X, W, labels, reduction="sum", grad=0.5)
