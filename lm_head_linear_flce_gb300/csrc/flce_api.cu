@@ -3,6 +3,7 @@
 // sequences of flce_forward / flce_backward.  See include/flce.h.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
@@ -190,6 +191,16 @@ void prof_end(int kind, int launches, cudaStream_t s) {
   g_prof.push_back(r);
 }
 
+// NVTX range over the host-side enqueue of one call (or one phase of it), so
+// that a timeline tool groups the call's launches; costs a pointer check when
+// no tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 #define FLCE_CUDA(x)                         \
   do {                                       \
     if ((x) != cudaSuccess) return FLCE_ERR_CUDA; \
@@ -315,6 +326,7 @@ flce_status forward_impl(const void* X, const void* W, const int64_t* labels, in
                          int64_t ignore_index, int shift, flce_reduction reduction, float* loss,
                          float* lse, float* z_out, int64_t* n_valid, void* workspace,
                          size_t workspace_bytes, flce_stream_t stream) {
+  NvtxRange range(z_out ? "flce_forward_vocab_shard" : "flce_forward");
   Plan p;
   flce_status st = check_common(X, W, labels, N, H, V, seq_len, shift, reduction, workspace,
                                 workspace_bytes, &p);
@@ -378,6 +390,8 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
                           const float* lse, const int64_t* n_valid, const float* grad_loss,
                           void* dX, float* dX_acc, void* dW, float* dW_acc, void* workspace,
                           size_t workspace_bytes, flce_stream_t stream) {
+  NvtxRange range(dX_acc ? "flce_backward_vocab_shard"
+                         : (dW_acc ? "flce_backward_accumulate" : "flce_backward"));
   Plan p;
   flce_status st = check_common(X, W, labels, N, H, V, seq_len, shift, reduction, workspace,
                                 workspace_bytes, &p);
@@ -525,6 +539,7 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
 
   // Launch p: recompute dZ block p (R tiles) while block p-1 is contracted
   // into dX (X tiles) and dW (W tiles).
+  NvtxRange gemm_range("backward GEMM launches");
   for (int lp = 0; lp <= nblk; ++lp) {
     BwdArgs a = base;
     a.counter = counters + lp;
@@ -610,6 +625,7 @@ flce_status flce_merge_vocab_shards(const float* lse_parts, const float* z_parts
                                     flce_reduction reduction, float* loss, float* lse,
                                     int64_t* n_valid, void* workspace, size_t workspace_bytes,
                                     flce_stream_t stream) {
+  NvtxRange range("flce_merge_vocab_shards");
   if (N < 0 || P <= 0 || P > kMaxShards || V_total <= 0) return FLCE_ERR_INVALID_ARG;
   if (N > kMaxDim || V_total > kMaxDim || P * N > kMaxDim) return FLCE_ERR_UNSUPPORTED_SHAPE;
   if (reduction != FLCE_REDUCTION_MEAN && reduction != FLCE_REDUCTION_SUM)
@@ -708,6 +724,7 @@ flce_status flce_backward_accumulate(const void* X, const void* W, const int64_t
 
 flce_status flce_logits(const void* X, const void* W, int64_t N, int64_t H, int64_t V,
                         void* logits, int64_t ld_logits, flce_stream_t stream) {
+  NvtxRange range("flce_logits");
   if (N < 0 || H <= 0 || V <= 0) return FLCE_ERR_INVALID_ARG;
   if (H % 8 != 0 || H > kMaxH || N > kMaxDim || V > kMaxDim) return FLCE_ERR_UNSUPPORTED_SHAPE;
   if (N == 0) return FLCE_OK;
