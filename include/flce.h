@@ -314,7 +314,7 @@ flce_status flce_selftest_wait_timeout(int64_t limit_ns, void* workspace,
  *                   timeout).
  * The scratch is a fixed 16 MiB array in the library's device image (held by
  * every GPU that loads the library until the process exits); it fits
- *   16 + 8*N + 8*N*ceil(V/1024) + 8*(N/256 + 2) bytes (each term rounded up to
+ *   16 + 8*N + 8*N*ceil(V/1024) + 8*(N/32 + 2) bytes (each term rounded up to
  *   256): e.g. N = 8192 at V = 152064.
  * Larger problems are rejected with FLCE_ERR_WORKSPACE_TOO_SMALL before
  * anything is enqueued.  Allocates nothing: no cudaMalloc, cudaFree or

@@ -250,7 +250,7 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   p->off_part = off;
   off = align_up(off + static_cast<size_t>(p->v_units) * N * 8);
   p->off_lossp = off;
-  off = align_up(off + static_cast<size_t>(cdiv(N, 256) + 1) * 8);
+  off = align_up(off + static_cast<size_t>(cdiv(N, kMergeRows) + 1) * 8);
   p->off_fcnt = off;  // forward unit ticket
   off = align_up(off + 4);
   const size_t fwd_end = off;

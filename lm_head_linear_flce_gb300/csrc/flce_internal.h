@@ -12,6 +12,9 @@ namespace flce {
 // Bits of the device error word (first int of the workspace).
 constexpr int kErrLabel = 1;    // a target outside [0, V) that is not ignore_index
 constexpr int kErrTimeout = 2;  // a bounded wait ran out
+// Rows per block of the forward's log-sum-exp merge: the loss partials hold
+// one FP64 value per kMergeRows rows.
+constexpr int kMergeRows = 32;
 // Stored target of a valid row whose label lies in another vocabulary shard:
 // no column of this call matches it, so the row has softmax terms only.
 constexpr int kTargetElsewhere = 0x7fffffff;

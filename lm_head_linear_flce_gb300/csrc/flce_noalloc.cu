@@ -121,7 +121,8 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
   const size_t off_zt = off_t + up(static_cast<size_t>(N) * 4);
   const size_t off_part = off_zt + up(static_cast<size_t>(N) * 4);
   const size_t off_lossp = off_part + up(static_cast<size_t>(v_units) * N * 8);
-  const size_t off_cnt = off_lossp + up(static_cast<size_t>((N + 255) / 256 + 1) * 8);
+  const size_t off_cnt =
+      off_lossp + up(static_cast<size_t>((N + kMergeRows - 1) / kMergeRows + 1) * 8);
   const size_t need = off_cnt + up(4);
   if (need > kNoallocScratchBytes) return FLCE_ERR_WORKSPACE_TOO_SMALL;
 

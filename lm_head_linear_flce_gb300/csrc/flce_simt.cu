@@ -9,7 +9,8 @@ namespace flce {
 namespace {
 
 constexpr int kPrepThreads = 256;
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 256;  // rows per block of the shard merge
+constexpr int kMergeGroups = 8;     // warps per block of the log-sum-exp merge
 constexpr int kFinalThreads = 256;
 
 // Effective target of every row after the optional per-sequence shift (the
@@ -66,24 +67,48 @@ __device__ __forceinline__ void block_loss_sum(double row_loss, double* red,
 }
 
 // lse_i = M + log sum_k s_k exp(m_k - M) over the forward's per-unit partials
-// (m_k, s_k); row loss = lse_i - z_{i,t_i} for valid rows.  Each block writes
-// the sum of its rows' losses.  With z_out (a vocabulary shard), lse is this
-// shard's log-sum-exp, z_out its target logit (0 where the target lies in
-// another shard) and no loss is formed.
-__global__ void merge_lse_kernel(const float2* __restrict__ partials, int nchunks, int N,
-                                 const float* __restrict__ zt, const int* __restrict__ targets,
-                                 float* __restrict__ lse, double* __restrict__ loss_partials,
-                                 float* __restrict__ z_out) {
-  __shared__ double red[kMergeThreads];
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+// (m_k, s_k); row loss = lse_i - z_{i,t_i} for valid rows.  A block takes
+// kMergeRows rows; each of its kMergeGroups warps merges every kMergeGroups-th
+// partial of those rows in one pass (a running max and rescaled sum; the
+// reads of a warp are 32 consecutive rows of one partial), then the first warp
+// combines the groups and writes the FP64 sum of its rows' losses (fixed
+// order).  With z_out (a vocabulary shard), lse is this shard's log-sum-exp,
+// z_out its target logit (0 where the target lies in another shard) and no
+// loss is formed.
+__global__ void __launch_bounds__(kMergeRows * kMergeGroups)
+    merge_lse_kernel(const float2* __restrict__ partials, int nchunks, int N,
+                     const float* __restrict__ zt, const int* __restrict__ targets,
+                     float* __restrict__ lse, double* __restrict__ loss_partials,
+                     float* __restrict__ z_out) {
+  __shared__ float2 grp[kMergeGroups][kMergeRows];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int i = blockIdx.x * kMergeRows + tx;
+  float m = -INFINITY, sum = 0.f;
+  if (i < N) {
+    // every partial has a finite max (each unit holds at least one column)
+    for (int k = ty; k < nchunks; k += kMergeGroups) {
+      const float2 p = partials[static_cast<size_t>(k) * N + i];
+      if (p.x > m) {
+        sum = sum * expf(m - p.x) + p.y;
+        m = p.x;
+      } else {
+        sum += p.y * expf(p.x - m);
+      }
+    }
+  }
+  grp[ty][tx] = make_float2(m, sum);
+  __syncthreads();
+  if (ty != 0) return;
   double row_loss = 0.0;
   if (i < N) {
-    float M = -INFINITY;
-    for (int k = 0; k < nchunks; ++k) M = fmaxf(M, partials[static_cast<size_t>(k) * N + i].x);
+    float M = grp[0][tx].x;
+#pragma unroll
+    for (int g = 1; g < kMergeGroups; ++g) M = fmaxf(M, grp[g][tx].x);
     float S = 0.f;
-    for (int k = 0; k < nchunks; ++k) {
-      const float2 p = partials[static_cast<size_t>(k) * N + i];
-      S += p.y * expf(p.x - M);
+#pragma unroll
+    for (int g = 0; g < kMergeGroups; ++g) {
+      const float2 q = grp[g][tx];
+      if (q.y != 0.f) S += q.y * expf(q.x - M);
     }
     const float l = M + logf(S);
     lse[i] = l;
@@ -92,7 +117,10 @@ __global__ void merge_lse_kernel(const float2* __restrict__ partials, int nchunk
     if (z_out) z_out[i] = here ? zt[i] : 0.f;
     else if (here) row_loss = static_cast<double>(l) - static_cast<double>(zt[i]);
   }
-  if (!z_out) block_loss_sum(row_loss, red, loss_partials);
+  if (z_out) return;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) row_loss += __shfl_down_sync(0xffffffffu, row_loss, off);
+  if (tx == 0) loss_partials[blockIdx.x] = row_loss;
 }
 
 // Merge of P vocabulary shards (Megatron-LM PR #2739, section 1: the vocabulary
@@ -224,11 +252,11 @@ cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int s
 cudaError_t launch_merge_lse(const float2* partials, int nchunks, int N, const float* zt,
                              const int* targets, float* lse, double* loss_partials,
                              cudaStream_t st, int* nblocks_out, float* z_out) {
-  const int blocks = (N + kMergeThreads - 1) / kMergeThreads;
+  const int blocks = (N + kMergeRows - 1) / kMergeRows;
   *nblocks_out = blocks;
   if (blocks == 0) return cudaSuccess;
-  merge_lse_kernel<<<blocks, kMergeThreads, 0, st>>>(partials, nchunks, N, zt, targets, lse,
-                                                     loss_partials, z_out);
+  merge_lse_kernel<<<blocks, dim3(kMergeRows, kMergeGroups), 0, st>>>(
+      partials, nchunks, N, zt, targets, lse, loss_partials, z_out);
   note_launch();
   return cudaGetLastError();
 }
