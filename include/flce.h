@@ -261,11 +261,14 @@ void flce_set_wait_limit_ns(int64_t limit_ns);
 
 /*
  * Tuning: caps the backward's dZ block at `max_rows` token rows (rounded down
- * to a multiple of 256, at least 256) and `max_block_elems` bf16 elements
- * (default 8192 rows and 32 Mi elements, a 64 MB block).
- * Smaller blocks mean less workspace and more FP32 accumulation traffic.
- * Values <= 0 restore the defaults.  Process-wide; flce_workspace_size and the
- * calls that use the workspace must see the same setting.
+ * to a multiple of 256, at least 256) and `max_block_elems` bf16 elements.
+ * A value <= 0 leaves that cap automatic: at most 32 Mi elements (a 64 MB
+ * block) when N <= 8192 and 64 Mi (128 MB) above, and every token row in one
+ * block while that leaves at least 2048 vocab columns per block (so dW is
+ * written once, with no FP32 accumulator across token blocks).  Smaller
+ * blocks mean less workspace and more FP32 accumulation traffic.
+ * Process-wide; flce_workspace_size and the calls that use the workspace must
+ * see the same setting.
  */
 void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems);
 

@@ -21,14 +21,20 @@ namespace {
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;
 constexpr int64_t kMaxH = 1 << 16;
 constexpr int64_t kMaxShards = 1 << 16;
-constexpr int64_t kDefaultDzBlockElems = int64_t{32} << 20;  // bf16 dZ block: 64 MB
-constexpr int64_t kDefaultMaxBlockRows = 8192;
+// Automatic backward blocking (no flce_set_backward_block caps): every token
+// row in one block while that leaves at least 2048 vocab columns, so that dW
+// is written once with no FP32 band; a dZ block of at most 32 Mi elements
+// (64 MB) up to 8192 rows and 64 Mi (128 MB) above.
+constexpr int64_t kSmallDzBlockElems = int64_t{32} << 20;
+constexpr int64_t kLargeDzBlockElems = int64_t{64} << 20;
+constexpr int64_t kSmallBlockRows = 8192;
+constexpr int64_t kMinBlockCols = 2048;
 constexpr size_t kAlign = 256;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
-std::atomic<int64_t> g_block_rows{kDefaultMaxBlockRows};
-std::atomic<int64_t> g_block_elems{kDefaultDzBlockElems};
+std::atomic<int64_t> g_block_rows{0};   // 0: automatic
+std::atomic<int64_t> g_block_elems{0};  // 0: automatic
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -221,11 +227,15 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   p->v_units = static_cast<int>(cdiv(p->v_tiles, kFwdGroup));
   p->h_tiles = static_cast<int>(cdiv(H, kBN));
   // Backward blocking: a token block of Nb rows x a vocab block of Vb columns
-  // of dZ is formed at a time (bf16, at most kDzBlockElems).  All rows in one
+  // of dZ is formed at a time (bf16, at most max_elems).  All rows in one
   // block when they fit, so dW needs no FP32 accumulator across blocks.
-  const int64_t max_rows = g_block_rows.load();
-  const int64_t max_elems = g_block_elems.load();
   const int64_t n_pad = std::max<int64_t>(int64_t{p->m_tiles} * kPairM, kPairM);
+  int64_t max_elems = g_block_elems.load();
+  if (max_elems <= 0)
+    max_elems = n_pad <= kSmallBlockRows ? kSmallDzBlockElems : kLargeDzBlockElems;
+  int64_t max_rows = g_block_rows.load();
+  if (max_rows <= 0)
+    max_rows = std::max<int64_t>(max_elems / kMinBlockCols / kPairM * kPairM, kPairM);
   if (n_pad <= max_rows) {
     p->Nb = n_pad;
   } else {
@@ -310,9 +320,8 @@ void flce_set_wait_limit_ns(int64_t limit_ns) {
 }
 
 void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems) {
-  g_block_rows.store(max_rows > 0 ? std::max<int64_t>(max_rows / kPairM * kPairM, kPairM)
-                                  : kDefaultMaxBlockRows);
-  g_block_elems.store(max_block_elems > 0 ? max_block_elems : kDefaultDzBlockElems);
+  g_block_rows.store(max_rows > 0 ? std::max<int64_t>(max_rows / kPairM * kPairM, kPairM) : 0);
+  g_block_elems.store(max_block_elems > 0 ? max_block_elems : 0);
 }
 
 }  // extern "C"

@@ -201,9 +201,13 @@ def test_shift_with_length_one_sequences_ignores_everything():
     assert got["n_valid"] == 0 and got["loss"] == 0.0
 
 
-def test_default_blocking_several_token_blocks():
-    # N above 8192 rows: two token blocks with the default backward blocking,
-    # so dW accumulates in the FP32 band and dX over several vocab blocks
+@pytest.mark.parametrize("blocks", [None, (8192, 32 << 20)])
+def test_more_than_8192_rows(blocks):
+    # automatic blocking: all 8492 rows in one token block (64 Mi-element dZ
+    # block); with 8192-row blocks: two token blocks, so dW accumulates in the
+    # FP32 band; dX over several vocab blocks either way
+    if blocks:
+        flce.flce_set_backward_block(*blocks)
     X, W, labels = workloads.random_case(8192 + 300, 64, 9000, seed=32, w_std=0.2)
     check_against_oracle(X, W, labels, seq_len=8492, shift=True)
 
@@ -238,9 +242,11 @@ def test_only_last_tile_active():
     (200, 16384, 600),     # long K for the recompute and for the dX / dW tiles' H sweep
     (64, 65536, 300),      # the largest supported H
     (40, 64, 300001),      # a vocabulary of 300K (many vocab blocks and forward units)
-    (20000, 32, 700),      # three token blocks at the default blocking, ragged last block
+    (20000, 32, 700),      # three ragged token blocks of at most 8192 rows
 ])
 def test_large_extents(N, H, V):
+    if N > 8192:
+        flce.flce_set_backward_block(8192, 32 << 20)
     X, W, labels = workloads.random_case(N, H, V, seed=N % 97 + H % 89 + V % 83,
                                          w_std=0.5 / np.sqrt(H) * 8)
     check_against_oracle(X, W, labels, reduction="sum", grad=0.5)
