@@ -53,12 +53,22 @@ KERNEL_SOURCES = [os.path.join(ROOT, "lm_head_linear_flce_gb300", "csrc", f)
                   for f in ("flce_gemm.cu", "flce_api.cu")]
 
 
+def _code_only(text: str) -> str:
+    """C++ source with comments and blank or trailing space removed (the sources
+    hold no string literal containing a comment marker)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_digest() -> str:
+    """sha256 (first 16 hex) of the kernel and launch sources, comments aside."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,6 +1,6 @@
 // Persistent tcgen05 GEMM kernels for the fused linear cross-entropy.
 //
-// Tile kinds (see GemmKind):
+// Tile kinds (the backward's three are GemmKind):
 //   FWD  Z = X W^T, epilogue: online log-sum-exp over the tile's vocab columns
 //        and the target-logit gather (the vocabulary split of Megatron-LM PR
 //        #2739 "[Dev] Fix Linear-Cross-Entropy Convergence Issue", section 2,

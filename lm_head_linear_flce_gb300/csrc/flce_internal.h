@@ -10,7 +10,7 @@
 namespace flce {
 
 // Bits of the device error word (first int of the workspace).
-constexpr int kErrLabel = 1;    // a target outside [0, V) that is not ignore_index
+constexpr int kErrLabel = 1;    // a target outside the vocabulary that is not ignore_index
 constexpr int kErrTimeout = 2;  // a bounded wait ran out
 // Rows per block of the forward's log-sum-exp merge: the loss partials hold
 // one FP64 value per kMergeRows rows.
@@ -54,7 +54,7 @@ enum GemmKind : int {
 struct GemmArgs {
   int tiles_m, tiles_n, group, units, k_blocks;
   int N, H, V;
-  const int* targets;  // [N], -1 = no valid target
+  const int* targets;  // [N]: local column, -1 (no valid target) or kTargetElsewhere
   float2* partials;    // [units_n][N]: per-row (max, sum exp(z - max)) over a work unit
   float* zt;           // [N]: target logit
   int* counter;        // unit ticket counter (starts at 0); loss forward only
