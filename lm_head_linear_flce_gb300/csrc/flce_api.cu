@@ -789,7 +789,8 @@ flce_status flce_profile_collect(double* ms, int64_t* launches) {
   flce_status st = FLCE_OK;
   for (const ProfRec& r : g_prof) {
     float t = 0.f;
-    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+    if (cudaEventSynchronize(r.b) != cudaSuccess ||
+        cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
       st = FLCE_ERR_CUDA;
     if (r.kind >= 0 && r.kind < 4) {
       if (ms) ms[r.kind] += t;

@@ -128,7 +128,8 @@ __device__ __forceinline__ void raise_error(int* err, int code) {
 // Wait until the phase with the given parity of `bar` has completed.  Returns
 // false (after recording a timeout and raising the abort flag) if it did not
 // complete within the limit, or if another warp of this CTA already aborted.
-static __device__ __noinline__ bool wait_parity_slow(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+static __device__ __noinline__ bool wait_parity_slow(uint32_t bar, uint32_t parity,
+                                                     const WaitCtx& w) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;

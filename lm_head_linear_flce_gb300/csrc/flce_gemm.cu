@@ -818,12 +818,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 // ================================================================= launchers
 namespace {
 
-// CTA pairs of `kernel` that fit on the device at once (cached per kernel).
-int max_pairs(const void* kernel, int smem, int* cache) {
-  if (*cache > 0) return *cache;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+constexpr int kMaxDevices = 64;
+
+// Per-kernel launch set-up, per device: the CTA pairs that fit at once (0
+// until the device's first launch).
+struct LaunchCache {
+  int pairs[kMaxDevices] = {};
+};
+
+// On the current device's first launch of `kernel`: raises its dynamic
+// shared-memory limit to `smem` and counts the CTA pairs that fit at once.
+// Later launches on that device read the count from `cache`.
+cudaError_t prepare_launch(const void* kernel, int smem, LaunchCache* cache, int* pairs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && cache->pairs[dev] > 0) {
+    *pairs = cache->pairs[dev];
+    return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -840,8 +859,9 @@ int max_pairs(const void* kernel, int smem, int* cache) {
     cudaGetLastError();
     n = sms / 2;
   }
-  *cache = n;
-  return n;
+  if (cached) cache->pairs[dev] = n;
+  *pairs = n;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -849,18 +869,12 @@ int max_pairs(const void* kernel, int smem, int* cache) {
 cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const GemmArgs& a,
                             int units, cudaStream_t st) {
   if (units <= 0) return cudaSuccess;
-  static bool attr = false;
-  static int pairs = 0;
+  static LaunchCache cache;
   auto* k = flce_fwd_kernel<kFwdLse>;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const int n =
-      std::min(units, max_pairs(reinterpret_cast<const void*>(k), kGemmSmemBytes, &pairs));
-  k<<<2 * n, kGemmThreads, kGemmSmemBytes, st>>>(tx, tw, tx, a);
+  int pairs = 0;
+  cudaError_t e = prepare_launch(reinterpret_cast<const void*>(k), kGemmSmemBytes, &cache, &pairs);
+  if (e != cudaSuccess) return e;
+  k<<<2 * std::min(units, pairs), kGemmThreads, kGemmSmemBytes, st>>>(tx, tw, tx, a);
   note_launch();
   return cudaGetLastError();
 }
@@ -869,18 +883,12 @@ cudaError_t launch_logits_gemm(const CUtensorMap& tx, const CUtensorMap& tw,
                                const CUtensorMap& tout, const GemmArgs& a, int units,
                                cudaStream_t st) {
   if (units <= 0) return cudaSuccess;
-  static bool attr = false;
-  static int pairs = 0;
+  static LaunchCache cache;
   auto* k = flce_fwd_kernel<kFwdLogits>;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const int n =
-      std::min(units, max_pairs(reinterpret_cast<const void*>(k), kBwdSmemBytes, &pairs));
-  k<<<2 * n, kGemmThreads, kBwdSmemBytes, st>>>(tx, tw, tout, a);
+  int pairs = 0;
+  cudaError_t e = prepare_launch(reinterpret_cast<const void*>(k), kBwdSmemBytes, &cache, &pairs);
+  if (e != cudaSuccess) return e;
+  k<<<2 * std::min(units, pairs), kGemmThreads, kBwdSmemBytes, st>>>(tx, tw, tout, a);
   note_launch();
   return cudaGetLastError();
 }
@@ -888,17 +896,12 @@ cudaError_t launch_logits_gemm(const CUtensorMap& tx, const CUtensorMap& tw,
 cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, bool overlap_prior,
                             cudaStream_t st) {
   if (units <= 0) return cudaSuccess;
-  static bool attr = false;
-  static int pairs = 0;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(flce_bwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kBwdSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const int n = std::min(units, max_pairs(reinterpret_cast<const void*>(flce_bwd_kernel),
-                                          kBwdSmemBytes, &pairs));
+  static LaunchCache cache;
+  int pairs = 0;
+  cudaError_t e0 = prepare_launch(reinterpret_cast<const void*>(flce_bwd_kernel), kBwdSmemBytes,
+                                  &cache, &pairs);
+  if (e0 != cudaSuccess) return e0;
+  const int n = std::min(units, pairs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * n, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
