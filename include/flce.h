@@ -241,9 +241,9 @@ flce_status flce_downcast_bf16(const float* src, void* dst, int64_t count,
 
 /*
  * Synchronises `stream`, then reads and returns the device error word written
- * by the last flce_forward / flce_backward call that used this workspace:
- * FLCE_OK, FLCE_ERR_LABEL_OUT_OF_RANGE or FLCE_ERR_TIMEOUT (the first one
- * raised wins; a timeout outranks a label error).  FLCE_ERR_CUDA if the
+ * by the last call that used this workspace (each call taking a workspace
+ * resets the word when it starts): FLCE_OK, FLCE_ERR_LABEL_OUT_OF_RANGE or
+ * FLCE_ERR_TIMEOUT (a timeout outranks a label error).  FLCE_ERR_CUDA if the
  * synchronisation itself fails.
  */
 flce_status flce_get_error(const void* workspace, flce_stream_t stream);
