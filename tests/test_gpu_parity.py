@@ -250,3 +250,26 @@ def test_large_extents(N, H, V):
     X, W, labels = workloads.random_case(N, H, V, seed=N % 97 + H % 89 + V % 83,
                                          w_std=0.5 / np.sqrt(H) * 8)
     check_against_oracle(X, W, labels, reduction="sum", grad=0.5)
+
+
+@pytest.mark.parametrize("name", ["qwen3_8b", "long_ctx", "stress"])
+def test_reduced_workloads_keep_their_distributions(name):
+    # each workload's own generator (Zipf labels with prompt spans, a masked
+    # prefix, wide logits) at a size the oracle finishes quickly
+    wl = workloads.get(name)
+    X, W, labels = workloads.make_inputs(wl, N=1024 * wl.B, H=256, V=3000, seed=77)
+    check_against_oracle(X, W, labels, seq_len=X.shape[0] // wl.B, shift=wl.shift,
+                         reduction=wl.reduction, grad=0.5)
+
+
+def test_every_target_the_same_class():
+    X, W, labels = workloads.random_case(600, 96, 1300, seed=78, ignore_frac=0.0)
+    labels[:] = 777
+    check_against_oracle(X, W, labels, reduction="sum")
+
+
+def test_two_token_sequences_with_shift():
+    # seq_len 2: only the first row of every pair has a target
+    X, W, labels = workloads.random_case(512, 64, 800, seed=79, ignore_frac=0.0)
+    got, ref = check_against_oracle(X, W, labels, seq_len=2, shift=True)
+    assert got["n_valid"] == 256
