@@ -424,6 +424,102 @@ def cpu_baseline(wl, X, W, L, rows: int):
                       "float64 forward + backward incl. their dW contribution"}
 
 
+# ------------------------------------------------- the other rows of the path
+ROWS = ("main", "dx_only", "accumulate", "logits", "vocab_shard4")
+
+
+def run_row(args, world, rank, local):
+    """One of the path's other entry points on the workload, timed like the
+    main step: dx_only (forward + backward without dW), accumulate (forward +
+    backward adding dW into an FP32 gradient), logits (plain bf16 logits, no
+    labels), vocab_shard4 (one rank of a four-way vocabulary split: shard
+    forward, merge, shard backward into an FP32 dX buffer; the all-gather and
+    all-reduce of a real group are not part of one GPU's step)."""
+    import lm_head_linear_flce_gb300 as flce
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = workloads.get(args.workload)
+    N, H, V = wl.N, wl.H, wl.V
+    X, W, L = (t.to(dev) for t in workloads.make_inputs(wl))
+    kw = dict(seq_len=wl.S, shift=wl.shift, reduction=wl.reduction)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+    if args.row == "vocab_shard4":
+        from lm_head_linear_flce_gb300.vocab_parallel import vocab_shard_bounds
+        v0, Vr = vocab_shard_bounds(V, 4)[0]
+        Wr = W[v0:v0 + Vr].contiguous()
+        del W
+        ws = torch.empty(flce.workspace_size(N, H, Vr), dtype=torch.uint8, device=dev)
+        dX_acc = torch.empty(N, H, dtype=torch.float32, device=dev)
+        dWr = torch.empty_like(Wr)
+        flops = 8 * N * H * Vr
+
+        def step():
+            lse_r, z_r, _, _ = flce.flce_forward_vocab_shard(X, Wr, L, v0, V, workspace=ws,
+                                                             seq_len=wl.S, shift=wl.shift)
+            # the gathered rows of four ranks (this rank's, four times: same cost)
+            loss, lse, nv = flce.flce_merge_vocab_shards(
+                lse_r.expand(4, N).contiguous(), z_r.expand(4, N).contiguous(), L, V,
+                workspace=ws, **kw)
+            dX_acc.zero_()
+            flce.flce_backward_vocab_shard(X, Wr, L, v0, V, lse, nv, g, dX_acc, workspace=ws,
+                                           dW=dWr, **kw)
+    else:
+        ws = torch.empty(flce.workspace_size(N, H, V), dtype=torch.uint8, device=dev)
+        dX = torch.empty_like(X)
+        if args.row == "dx_only":
+            flops = 6 * N * H * V
+
+            def step():
+                _, lse, nv, _ = flce.flce_forward(X, W, L, workspace=ws, **kw)
+                flce.flce_backward(X, W, L, lse, nv, g, workspace=ws, dX=dX, need_dW=False, **kw)
+        elif args.row == "accumulate":
+            flops = 8 * N * H * V
+            dW_acc = torch.zeros(V, H, dtype=torch.float32, device=dev)
+
+            def step():
+                _, lse, nv, _ = flce.flce_forward(X, W, L, workspace=ws, **kw)
+                flce.flce_backward_accumulate(X, W, L, lse, nv, g, dW_acc, workspace=ws, dX=dX,
+                                              **kw)
+        else:  # logits
+            flops = 2 * N * H * V
+            del ws
+
+            def step():
+                flce.flce_logits(X, W)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = flce.flce_kernel_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = flce.flce_kernel_launch_count() - n0
+    value, worst = aggregate_throughput(N, args.steps, t0.elapsed_time(t1), world, dev)
+    ms_step = worst / args.steps
+    peaks, src = load_peaks()
+    tfl = flops / (ms_step / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "row": args.row, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "N": N, "H": H, "V": V, "row": args.row},
+            "roofline": {"kernel": "step", "bound": "tensor", "achieved": round(tfl, 1),
+                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": round(tfl / peaks["bf16_tflops_sustained"], 4),
+                         "traffic": None, "flops_per_step": flops,
+                         "peak_source": f"bf16_tflops_sustained ({src})"},
+            "gpu_launches": launches}), flush=True)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -466,6 +562,9 @@ def main(argv=None):
     p.add_argument("--ref-rows", type=int, default=8)
     p.add_argument("--tokens", type=int, default=0, help="override N (profiling cases)")
     p.add_argument("--vocab", type=int, default=0, help="override V (profiling cases)")
+    p.add_argument("--row", default="main", choices=ROWS,
+                   help="main: the fused forward + backward step; the others time the path's "
+                        "other entry points")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -473,6 +572,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.row != "main":
+            run_row(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:
