@@ -144,6 +144,13 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p);
 // Counts one kernel launch (see flce_kernel_launch_count).
 void note_launch();
 
+// 2-D tensor map over a row-major [outer][inner] matrix (rows `row_bytes`
+// apart) with 128-byte swizzle and the given box; out-of-bounds elements read
+// as zero and are not written.  False if the driver rejects it.
+bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+
 // The vocabulary columns a call holds: [v_offset, v_offset + V_local) of a
 // V_total-column vocabulary (the whole of it outside the vocabulary-parallel
 // entry points).

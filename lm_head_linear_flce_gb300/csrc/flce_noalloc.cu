@@ -62,33 +62,6 @@ flce_status setup_device(int dev, void** scratch) {
   return FLCE_OK;
 }
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-bool encode_bf16_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
-                     uint32_t box_inner, uint32_t box_outer) {
-  static EncodeFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<EncodeFn>(nullptr);
-    return reinterpret_cast<EncodeFn>(p);
-  }();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 }  // namespace flce
 
@@ -152,7 +125,8 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
                             err, s) != cudaSuccess)
       return FLCE_ERR_CUDA;
     CUtensorMap tx, tw;
-    if (!encode_bf16_map(&tx, X, H, N, kBK, kBM) || !encode_bf16_map(&tw, W, H, V, kBK, kHalfN))
+    if (!make_tmap(&tx, X, H, N, H * 2, kBK, kBM) ||
+        !make_tmap(&tw, W, H, V, H * 2, kBK, kHalfN))
       return FLCE_ERR_CUDA;
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
