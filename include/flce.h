@@ -69,9 +69,10 @@ typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 } flce_reduction;
 /*
  * Bytes of device workspace flce_forward and flce_backward need for these
  * sizes (one buffer serves both; it need not survive from forward to
- * backward).  It is O(N*H + Vb*H + N*V/1024 + tiles), never O(N*V): FP32
+ * backward).  It is O(N*H + Vb*H + 128*N + tiles), never O(N*V): FP32
  * accumulators for dX and for one vocab band of dW, a bounded bf16 block of
- * dZ, and per-row partial log-sum-exps.  Returns 0 for invalid sizes.
+ * dZ, and per-row partial log-sum-exps (at most 128 per row, whatever V is).
+ * Returns 0 for invalid sizes.
  */
 size_t flce_workspace_size(int64_t N, int64_t H, int64_t V);
 
@@ -253,9 +254,9 @@ const char* flce_status_string(flce_status status);
 
 /*
  * Limit, in nanoseconds, on every wait inside the library's kernels (default
- * 2e9).  A wait that runs out records FLCE_ERR_TIMEOUT and its kernel returns
- * early.  Values <= 0 restore the default.  Process-wide; not thread-safe
- * against concurrent calls.
+ * 2e9), flce_forward_noalloc's included; it applies to calls made after it is
+ * set.  A wait that runs out records FLCE_ERR_TIMEOUT and its kernel returns
+ * early.  Values <= 0 restore the default.  Process-wide.
  */
 void flce_set_wait_limit_ns(int64_t limit_ns);
 
@@ -278,6 +279,10 @@ void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems);
  * flce_kernel_launch_count: kernels this library has launched in this process
  * (tensor-core GEMMs and the small SIMT kernels; memsets not included).
  *
+ * flce_last_launch_wait_limit_ns: the wait limit (ns) the most recent
+ * tensor-core launch of any entry point was given (0 before the first), so a
+ * caller can check that flce_set_wait_limit_ns reached the kernels.
+ *
  * flce_profile_enable(1) makes later calls record CUDA events on the call's
  * stream around their tensor-core launches (events come from a pool the
  * library owns; no device memory is allocated): around the forward GEMM
@@ -290,6 +295,7 @@ void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems);
  * or FLCE_ERR_CUDA.  flce_profile_enable(0) stops recording.
  */
 int64_t flce_kernel_launch_count(void);
+int64_t flce_last_launch_wait_limit_ns(void);
 void flce_profile_enable(int enable);
 flce_status flce_profile_collect(double* ms, int64_t* launches);
 
@@ -315,10 +321,16 @@ flce_status flce_selftest_wait_timeout(int64_t limit_ns, void* workspace,
  *   device_error    device int, 1 element, or NULL: receives this call's
  *                   device error bits (0 none, 1 label out of range, 2 wait
  *                   timeout).
- * The scratch is a fixed 16 MiB array in the library's device image (held by
- * every GPU that loads the library until the process exits); it fits
- *   16 + 8*N + 8*N*ceil(V/1024) + 8*(N/32 + 2) bytes (each term rounded up to
- *   256): e.g. N = 8192 at V = 152064.
+ * The scratch is a fixed 16 MiB (16777216-byte) array in the library's device
+ * image (held by every GPU that loads the library until the process exits).
+ * A call needs, with up(x) = x rounded up to a multiple of 256,
+ *     256                        error word
+ *   + 2 * up(4 * N)              targets, target logits
+ *   + up(8 * N * U)              per-row (max, sum-exp) of each work unit
+ *   + up(8 * (ceil(N / 32) + 1)) per-block loss sums
+ *   + 256                        work-unit counter
+ * bytes, where T = ceil(V / 256) and U = ceil(T / max(4, ceil(T / 128))) <= 128
+ * (U = 119 at V = 151936 or 152064): e.g. N = 16384 at V = 151936 fits.
  * Larger problems are rejected with FLCE_ERR_WORKSPACE_TOO_SMALL before
  * anything is enqueued.  Allocates nothing: no cudaMalloc, cudaFree or
  * allocating library call.  The first call on a device looks up the scratch

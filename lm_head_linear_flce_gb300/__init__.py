@@ -21,7 +21,8 @@ import torch
 __all__ = [
     "FlceError", "library", "library_path", "workspace_size", "flce_forward", "flce_backward",
     "flce_get_error", "flce_selftest_wait_timeout", "flce_set_wait_limit_ns",
-    "flce_set_backward_block", "flce_kernel_launch_count", "flce_profile_enable",
+    "flce_set_backward_block", "flce_kernel_launch_count", "flce_last_launch_wait_limit_ns",
+    "flce_profile_enable",
     "flce_profile_collect", "PROFILE_KINDS", "flce_forward_noalloc", "flce_backward_accumulate",
     "flce_logits", "flce_forward_vocab_shard", "flce_merge_vocab_shards",
     "flce_backward_vocab_shard", "flce_downcast_bf16",
@@ -329,6 +330,14 @@ def flce_kernel_launch_count() -> int:
     return int(library().flce_kernel_launch_count())
 
 
+def flce_last_launch_wait_limit_ns() -> int:
+    """The wait limit (ns) the most recent tensor-core launch was given."""
+    fn = library().flce_last_launch_wait_limit_ns
+    fn.argtypes = []
+    fn.restype = ctypes.c_int64
+    return int(fn())
+
+
 def flce_profile_enable(enable: bool) -> None:
     library().flce_profile_enable(int(bool(enable)))
 
@@ -358,7 +367,8 @@ def flce_forward_noalloc(X, W, labels, *, seq_len=None, ignore_index=-100, shift
     """flce_forward without a workspace (C entry point flce_forward_noalloc).
 
     For callers that cannot allocate device memory: the library keeps a fixed
-    16 MiB scratch array in its device image and uses it instead.  Returns
+    16 MiB scratch array in its device image and uses it instead (problems
+    needing more are refused with FLCE_ERR_WORKSPACE_TOO_SMALL).  Returns
     (loss [1] f32, lse [N] f32, n_valid [1] i64, device_error [1] i32).  Calls
     share the scratch; serialise calls that could overlap on the GPU.
     """

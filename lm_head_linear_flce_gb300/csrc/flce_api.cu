@@ -44,26 +44,27 @@ struct DeviceInfo {
   bool ok = false;
 };
 
+// Per-device answer, cached: 0 until the first query on that device, then
+// (SM count << 1) | (compute capability is 10.3).  Atomic, so concurrent
+// first calls from several host threads are safe (they store the same value).
+std::atomic<int> g_device_cache[64];
+
 flce_status device_info(DeviceInfo* d) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
-  static DeviceInfo cache[64];
-  static bool have[64] = {};
-  if (dev >= 0 && dev < 64 && have[dev]) {
-    *d = cache[dev];
-    return d->ok ? FLCE_OK : FLCE_ERR_UNSUPPORTED_DEVICE;
+  const bool cacheable = dev >= 0 && dev < 64;
+  int v = cacheable ? g_device_cache[dev].load(std::memory_order_acquire) : 0;
+  if (v == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    v = (std::max(sms, 1) << 1) | ((major == 10 && minor == 3) ? 1 : 0);
+    if (cacheable) g_device_cache[dev].store(v, std::memory_order_release);
   }
-  int major = 0, minor = 0, sms = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return FLCE_ERR_CUDA;
-  d->sms = sms;
-  d->ok = (major == 10 && minor == 3);
-  if (dev >= 0 && dev < 64) {
-    cache[dev] = *d;
-    have[dev] = true;
-  }
+  d->sms = v >> 1;
+  d->ok = (v & 1) != 0;
   return d->ok ? FLCE_OK : FLCE_ERR_UNSUPPORTED_DEVICE;
 }
 
@@ -216,6 +217,14 @@ bool make_tmap_mn3(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t row
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+namespace {
+std::atomic<unsigned long long> g_last_wait_limit{0};
+}  // namespace
+
+void note_wait_limit(unsigned long long limit_ns) { g_last_wait_limit.store(limit_ns); }
+
 bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   if (N < 0 || H <= 0 || V <= 0) return false;
   std::memset(p, 0, sizeof(*p));
@@ -224,7 +233,8 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   p->V = V;
   p->m_tiles = static_cast<int>(cdiv(N, kPairM));
   p->v_tiles = static_cast<int>(cdiv(V, kBN));
-  p->v_units = static_cast<int>(cdiv(p->v_tiles, kFwdGroup));
+  p->fwd_group = forward_unit_tiles(p->v_tiles);
+  p->v_units = static_cast<int>(cdiv(p->v_tiles, p->fwd_group));
   p->h_tiles = static_cast<int>(cdiv(H, kBN));
   // Backward blocking: a token block of Nb rows x a vocab block of Vb columns
   // of dZ is formed at a time (bf16, at most max_elems).  All rows in one
@@ -258,7 +268,7 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   p->off_zt = off;
   off = align_up(off + static_cast<size_t>(N) * 4);
   p->off_part = off;
-  off = align_up(off + static_cast<size_t>(p->v_units) * N * 8);
+  off = align_up(off + static_cast<size_t>(kFwdSplits) * N * 8);  // O(N * splits), not O(N * V)
   p->off_lossp = off;
   off = align_up(off + static_cast<size_t>(cdiv(N, kMergeRows) + 1) * 8);
   p->off_fcnt = off;  // forward unit ticket
@@ -368,7 +378,7 @@ flce_status forward_impl(const void* X, const void* W, const int64_t* labels, in
   std::memset(&a, 0, sizeof(a));
   a.tiles_m = p.m_tiles;
   a.tiles_n = p.v_tiles;
-  a.group = kFwdGroup;
+  a.group = p.fwd_group;
   a.units = p.m_tiles * p.v_units;
   a.k_blocks = static_cast<int>(cdiv(H, kBK));
   a.N = static_cast<int>(N);
@@ -777,6 +787,10 @@ flce_status flce_get_error(const void* workspace, flce_stream_t stream) {
 }
 
 int64_t flce_kernel_launch_count(void) { return g_launches.load(); }
+
+int64_t flce_last_launch_wait_limit_ns(void) {
+  return static_cast<int64_t>(g_last_wait_limit.load());
+}
 
 void flce_profile_enable(int enable) { g_prof_on.store(enable != 0); }
 

@@ -40,6 +40,7 @@
 //   warps 2..5  epilogue: tcgen05.ld of this CTA's accumulator rows (warp w owns
 //               TMEM lanes 32*(w%4) .. +31), then the kind's epilogue.
 #include <algorithm>
+#include <atomic>
 
 #include "flce_device.cuh"
 #include "flce_internal.h"
@@ -821,9 +822,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 // Per-kernel launch set-up, per device: the CTA pairs that fit at once (0
-// until the device's first launch).
+// until the device's first launch).  Atomic: host threads may launch at once;
+// racing first launches each set the same attribute and store the same count.
 struct LaunchCache {
-  int pairs[kMaxDevices] = {};
+  std::atomic<int> pairs[kMaxDevices] = {};
 };
 
 // On the current device's first launch of `kernel`: raises its dynamic
@@ -834,9 +836,12 @@ cudaError_t prepare_launch(const void* kernel, int smem, LaunchCache* cache, int
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const bool cached = dev >= 0 && dev < kMaxDevices;
-  if (cached && cache->pairs[dev] > 0) {
-    *pairs = cache->pairs[dev];
-    return cudaSuccess;
+  if (cached) {
+    const int n = cache->pairs[dev].load(std::memory_order_acquire);
+    if (n > 0) {
+      *pairs = n;
+      return cudaSuccess;
+    }
   }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -859,7 +864,7 @@ cudaError_t prepare_launch(const void* kernel, int smem, LaunchCache* cache, int
     cudaGetLastError();
     n = sms / 2;
   }
-  if (cached) cache->pairs[dev] = n;
+  if (cached) cache->pairs[dev].store(n, std::memory_order_release);
   *pairs = n;
   return cudaSuccess;
 }
@@ -876,6 +881,7 @@ cudaError_t launch_fwd_gemm(const CUtensorMap& tx, const CUtensorMap& tw, const 
   if (e != cudaSuccess) return e;
   k<<<2 * std::min(units, pairs), kGemmThreads, kGemmSmemBytes, st>>>(tx, tw, tx, a);
   note_launch();
+  note_wait_limit(a.wait_limit_ns);
   return cudaGetLastError();
 }
 
@@ -890,6 +896,7 @@ cudaError_t launch_logits_gemm(const CUtensorMap& tx, const CUtensorMap& tw,
   if (e != cudaSuccess) return e;
   k<<<2 * std::min(units, pairs), kGemmThreads, kBwdSmemBytes, st>>>(tx, tw, tout, a);
   note_launch();
+  note_wait_limit(a.wait_limit_ns);
   return cudaGetLastError();
 }
 
@@ -914,6 +921,7 @@ cudaError_t launch_bwd_gemm(const BwdMaps& maps, const BwdArgs& a, int units, bo
   cfg.numAttrs = overlap_prior ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, flce_bwd_kernel, maps, a);
   note_launch();
+  note_wait_limit(a.wait_limit_ns);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -37,7 +37,12 @@ constexpr int kAccCols = kBN;   // FP32 accumulator columns per tile
 constexpr int kNumAcc = 2;      // double-buffered accumulators
 constexpr int kTmemCols = kAccCols * kNumAcc;  // 512: the whole tensor memory
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kFwdGroup = 4;    // vocab tiles merged per forward work unit
+constexpr int kFwdGroup = 4;    // fewest vocab tiles merged per forward work unit
+// Most forward work units per 256-row tile: each unit covers a contiguous run
+// of at least kFwdGroup vocab tiles and leaves one (max, sum-exp) partial per
+// row, so the partials are O(N * kFwdSplits) whatever V is.  128 keeps units
+// short enough (5 tiles at V = 152K) that the dynamic hand-out ends evenly.
+constexpr int kFwdSplits = 128;
 constexpr int kGemmSmemBytes = kStages * (kAStageBytes + kBStageBytes) + 1024 /*align*/ + 256;
 // backward epilogue staging: per epilogue warp two 4 KB buffers (32 rows x 128 B)
 constexpr int kStageBufBytes = 4096;
@@ -128,7 +133,9 @@ struct BwdArgs {
 // workspace layout.  Pure function of (N, H, V).
 struct Plan {
   int64_t N, H, V;
-  int m_tiles, v_tiles, v_units, h_tiles;
+  int m_tiles, v_tiles, h_tiles;
+  int fwd_group;          // vocab tiles per forward work unit
+  int v_units;            // forward work units per 256-row tile (<= kFwdSplits)
   int64_t Nb, Vb;         // backward block: token rows x vocab columns
   int64_t dz_ld;          // elements per dZ row in a slot (Vb plus padding)
   int n_blocks, v_blocks;
@@ -141,8 +148,21 @@ struct Plan {
 
 bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p);
 
+// Vocab tiles per forward work unit for a vocabulary of v_tiles 256-column
+// tiles: at least kFwdGroup, and few enough units (<= kFwdSplits) per row tile.
+inline int forward_unit_tiles(int64_t v_tiles) {
+  const int64_t by_splits = (v_tiles + kFwdSplits - 1) / kFwdSplits;
+  return static_cast<int>(by_splits > kFwdGroup ? by_splits : kFwdGroup);
+}
+
+// The limit every bounded wait of the next launches uses (flce_set_wait_limit_ns).
+unsigned long long wait_limit_ns();
+
 // Counts one kernel launch (see flce_kernel_launch_count).
 void note_launch();
+// Records the wait limit a tensor-core launch was given (see
+// flce_last_launch_wait_limit_ns).
+void note_wait_limit(unsigned long long limit_ns);
 
 // 2-D tensor map over a row-major [outer][inner] matrix (rows `row_bytes`
 // apart) with 128-byte swizzle and the given box; out-of-bounds elements read

@@ -31,7 +31,6 @@ namespace {
 constexpr size_t kNoallocScratchBytes = size_t{16} << 20;  // 16 MiB
 constexpr size_t kNoallocAlign = 256;
 constexpr int kMaxDevices = 64;
-constexpr unsigned long long kNoallocWaitNs = 2000000000ull;
 
 // Device-side scratch.  In host code this name is only a host-side stand-in
 // for the symbol: its device address comes from cudaGetSymbolAddress below.
@@ -86,10 +85,12 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     const int64_t S = seq_len > 0 ? seq_len : N;
     if (N % S != 0) return FLCE_ERR_INVALID_ARG;
   }
-  // scratch layout: error word | targets | target logits | lse partials | loss partials
+  // scratch layout (each piece starts on a 256-byte boundary): error word |
+  // targets | target logits | lse partials | loss partials | unit counter
   const int64_t m_tiles = (N + kPairM - 1) / kPairM;
   const int64_t v_tiles = (V + kBN - 1) / kBN;
-  const int64_t v_units = (v_tiles + kFwdGroup - 1) / kFwdGroup;
+  const int group = forward_unit_tiles(v_tiles);
+  const int64_t v_units = (v_tiles + group - 1) / group;
   const size_t off_t = up(16);
   const size_t off_zt = off_t + up(static_cast<size_t>(N) * 4);
   const size_t off_part = off_zt + up(static_cast<size_t>(N) * 4);
@@ -132,7 +133,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     std::memset(&a, 0, sizeof(a));
     a.tiles_m = static_cast<int>(m_tiles);
     a.tiles_n = static_cast<int>(v_tiles);
-    a.group = kFwdGroup;
+    a.group = group;
     a.units = static_cast<int>(m_tiles * v_units);
     a.k_blocks = static_cast<int>((H + kBK - 1) / kBK);
     a.N = static_cast<int>(N);
@@ -143,7 +144,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     a.zt = zt;
     a.counter = counter;
     a.err = err;
-    a.wait_limit_ns = kNoallocWaitNs;
+    a.wait_limit_ns = wait_limit_ns();  // flce_set_wait_limit_ns applies here too
     if (launch_fwd_gemm(tx, tw, a, a.units, s) != cudaSuccess)
       return FLCE_ERR_CUDA;
     int nblocks = 0;

@@ -171,6 +171,50 @@ def backward(X, W, labels, *, seq_len=None, shift=False, ignore_index=IGNORE_IND
     return dX, dW
 
 
+def forward_backward(X, W, labels, *, seq_len=None, shift=False, ignore_index=IGNORE_INDEX,
+                     reduction="mean", grad_loss=1.0, row_block=2048):
+    """forward() and backward() in one pass over the row blocks: each block's
+    logits Z = X_blk W^T are formed once and give that block's lse, target
+    logits, dZ, dX rows and its term dZ_blk^T X_blk of dW (the chunk sum of
+    PR #9784, section Mathematical Equivalence).  Same definition, same
+    arithmetic per block as the two functions; it only avoids forming Z twice,
+    which matters at the full workload sizes.
+
+    Returns a dict with the keys of forward() plus dX [N,H] and dW [V,H]
+    (float64).
+    """
+    Xd, Wd = as_f64(X), as_f64(W)
+    N, V = Xd.shape[0], Wd.shape[0]
+    t, valid, n_valid, oor = effective_targets(labels, V, seq_len=seq_len, shift=shift,
+                                               ignore_index=ignore_index)
+    s = grad_scale(reduction, n_valid, grad_loss)
+    lse = np.empty(N)
+    zt = np.full(N, np.nan)
+    dX = np.zeros_like(Xd)
+    dW = np.zeros_like(Wd)
+    for r0 in range(0, N, row_block):
+        r1 = min(N, r0 + row_block)
+        Z = Xd[r0:r1] @ Wd.T
+        l = _row_logsumexp(Z)
+        lse[r0:r1] = l
+        v = valid[r0:r1]
+        zt[r0:r1][v] = Z[np.nonzero(v)[0], t[r0:r1][v]]
+        dZ = grad_logits(Z, l, t[r0:r1], v, s)
+        del Z
+        dX[r0:r1] = dZ @ Wd
+        dW += dZ.T @ Xd[r0:r1]
+    row_loss = np.where(valid, lse - np.where(valid, zt, 0.0), 0.0)
+    total = float(row_loss.sum())
+    if reduction == "mean":
+        loss = total / n_valid if n_valid > 0 else 0.0
+    elif reduction == "sum":
+        loss = total
+    else:
+        raise ValueError(reduction)
+    return dict(loss=loss, lse=lse, row_loss=row_loss, z_target=zt, n_valid=n_valid,
+                out_of_range=oor, targets=t, valid=valid, dX=dX, dW=dW)
+
+
 # ---------------------------------------------------------------------------
 # Sampled outputs for full-size checks: each is the same definition restricted
 # to a few rows (of dX / lse) or a few vocab rows (of dW).

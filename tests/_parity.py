@@ -41,3 +41,22 @@ def assert_loss(got, ref):
 def assert_lse(got, ref):
     err = np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))
     assert err.max() <= LSE_ATOL, f"lse max abs err {err.max():.3e}"
+
+
+# Oracle forward results of the full-size workloads, kept for the rest of the
+# test session (loss, lse, n_valid: small) so that a later test on the same
+# workload need not redo minutes of host work.  Filled by whichever test
+# computes them first; oracle_forward_cached computes them when absent, so
+# every test also runs on its own.
+_ORACLE_FORWARD = {}
+
+
+def remember_oracle_forward(name, ref):
+    _ORACLE_FORWARD[name] = {k: ref[k] for k in ("loss", "lse", "n_valid", "valid")}
+
+
+def oracle_forward_cached(name, X, W, labels, **kw):
+    if name not in _ORACLE_FORWARD:
+        import oracle
+        remember_oracle_forward(name, oracle.forward(X, W, labels, **kw))
+    return _ORACLE_FORWARD[name]

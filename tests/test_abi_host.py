@@ -146,3 +146,45 @@ def test_vocab_shard_entry_points_reject_bad_arguments_on_host(lib):
     assert down(count=12) == 1
     assert down(count=0) == 0
     assert down(src=_fake(0x200008)) == 1
+
+
+def _noalloc_need(N, V):
+    """Scratch bytes of flce_forward_noalloc, as the header states them."""
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    T = -(-V // 256)
+    U = -(-T // max(4, -(-T // 128)))
+    assert U <= 128
+    return 256 + 2 * up(4 * N) + up(8 * N * U) + up(8 * (-(-N // 32) + 1)) + 256
+
+
+@pytest.mark.parametrize("V", [4096, 32768, 151936, 152064, 262144, 1 << 22])
+def test_noalloc_scratch_formula(lib, V):
+    """The largest N the header's formula lets into the 16 MiB scratch passes
+    the size check and one more row is refused, before anything is enqueued."""
+    import torch
+    cap = 16 << 20
+    lo, hi = 1, 1 << 20
+    while lo < hi:  # largest N with need(N) <= cap
+        mid = (lo + hi + 1) // 2
+        lo, hi = (mid, hi) if _noalloc_need(mid, V) <= cap else (lo, mid - 1)
+    n_max = lo
+    i64, c_int = ctypes.c_int64, ctypes.c_int
+    fn = lib.flce_forward_noalloc
+    fn.argtypes = [ctypes.c_void_p] * 3 + [i64] * 5 + [c_int, c_int] + [ctypes.c_void_p] * 5
+    fn.restype = c_int
+
+    def call(N):
+        return fn(_fake(), _fake(), _fake(), N, 8, V, 0, -100, 0, 0, _fake(), _fake(), _fake(),
+                  None, None)
+
+    assert call(n_max + 1) == 3
+    if not torch.cuda.is_available():
+        # passes the size check, then stops at the device query (no GPU here)
+        assert call(n_max) not in (0, 3)
+
+
+def test_forward_partials_do_not_grow_with_the_vocabulary(lib):
+    # at most 128 (max, sum-exp) partials per row whatever V is: with a
+    # vocabulary past 512 tiles the noalloc size limit no longer moves
+    assert _noalloc_need(8192, 1 << 22) == _noalloc_need(8192, 1 << 24)
+    assert _noalloc_need(8192, 152064) < _noalloc_need(8192, 1 << 22)

@@ -1,20 +1,30 @@
 """Parity at the full workload sizes, in the launch configuration bench.py times
-(default backward blocking).
+(default backward blocking), over whole matrices.
 
-For every workload the CPU oracle computes, in float64: the full forward (lse
-of every row, the loss, n_valid), dX for a sample of token rows (each needs
-its own full row of logits) and dW for a sample of vocab rows (each needs the
-oracle's lse of every token).  The rest of dW is checked through an identity
-that holds at any size: every row of dZ sums to zero, so the vocab rows of dW
-sum to the zero vector.
+For every workload the CPU oracle runs the unfused computation in float64 on
+the same bf16 inputs (one pass over row blocks: each block's full logits give
+its lse, its dX rows and its term of dW) and the CUDA path is compared with it
+on everything it returns: n_valid exactly, the loss, the lse of every row, all
+of dX (N x H) and all of dW (V x H) by relative Frobenius error and cosine.
+The pages' own equivalence check is a whole-gradient cosine (ms-swift PR
+#9784, section Mathematical Equivalence), and the stress workload exists to
+check FP32 accumulation of dX and dW across vocabulary slices (Megatron-LM PR
+#2739, section 2).
+
+A few sampled rows of dX and vocab rows of dW are checked first (cheap, and a
+gross error shows up before the minutes of host work the whole oracle takes).
+The measured errors are printed (run pytest with -s or -rA to see them).
 """
+import time
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads
-from tests._parity import assert_grad, assert_loss, assert_lse, to_np
+from tests._parity import (assert_grad, assert_loss, assert_lse, grad_metrics,
+                           remember_oracle_forward, to_np)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -49,28 +59,34 @@ def test_full_size_parity(name):
     del dX, dW, ws
     torch.cuda.empty_cache()
 
-    ref = oracle.forward(X, W, labels, **kw)
+    # fast pre-check on sampled rows (each needs only its own row of logits)
+    t, valid, n_valid, _ = oracle.effective_targets(labels, wl.V, seq_len=wl.S, shift=wl.shift)
+    assert got_nv == n_valid
+    rng = np.random.default_rng(7)
+    rows = pick_rows(valid, wl.S, wl.N, rng)
+    r = oracle.rows_forward_backward(X, W, labels, rows, grad_loss=g, **kw)
+    assert_lse(got_lse[rows], r["lse"])
+    assert_grad("dX sampled rows", to_np(dXh[torch.as_tensor(rows)]), r["dX"])
+
+    # the whole computation
+    t0 = time.perf_counter()
+    ref = oracle.forward_backward(X, W, labels, grad_loss=g, **kw)
+    host_s = time.perf_counter() - t0
+    remember_oracle_forward(name, ref)
     assert got_nv == ref["n_valid"]
     assert_loss(got_loss, ref["loss"])
     assert_lse(got_lse, ref["lse"])
-
-    rng = np.random.default_rng(7)
-    rows = pick_rows(ref["valid"], wl.S, wl.N, rng)
-    r = oracle.rows_forward_backward(X, W, labels, rows, grad_loss=g, **kw)
-    got_dx = to_np(dXh[torch.as_tensor(rows)])
-    assert_grad("dX rows", got_dx, r["dX"])
-    ign = ~ref["valid"][rows]
+    got_dx = to_np(dXh)
+    ign = ~ref["valid"]
     assert not got_dx[ign].any(), "ignored rows must have dX exactly 0"
-
-    tv = ref["targets"][ref["valid"]]
-    js = {0, wl.V - 1}
-    js.update(rng.choice(tv, 6, replace=False).tolist())
-    js.update(rng.integers(0, wl.V, 6).tolist())
-    js = np.array(sorted(js))
-    ref_dw = oracle.vocab_rows_dW(X, W, labels, ref["lse"], js, grad_loss=g, **kw)
-    assert_grad("dW rows", to_np(dWh[torch.as_tensor(js)]), ref_dw)
-
-    # sum over the vocabulary of dW is the zero vector (per-row sums of dZ vanish)
-    dW64 = dWh.double()
-    col = dW64.sum(0).norm().item()
-    assert col <= 1e-2 * dW64.norm().item(), col
+    dx_rel, dx_cos = grad_metrics(got_dx, ref["dX"])
+    del got_dx
+    ref.pop("dX")
+    dw_rel, dw_cos = grad_metrics(to_np(dWh), ref["dW"])
+    lse_err = float(np.abs(got_lse - ref["lse"]).max())
+    loss_rel = abs(got_loss - ref["loss"]) / abs(ref["loss"]) if ref["loss"] else 0.0
+    print(f"\nfull-size parity {name}: loss rel {loss_rel:.2e}, lse max abs {lse_err:.2e}, "
+          f"dX rel {dx_rel:.3e} cos {dx_cos:.8f}, dW rel {dw_rel:.3e} cos {dw_cos:.8f} "
+          f"(oracle {host_s:.0f} s on the host)")
+    assert dx_rel <= 1e-2 and dx_cos >= 0.9999, ("dX", dx_rel, dx_cos)
+    assert dw_rel <= 1e-2 and dw_cos >= 0.9999, ("dW", dw_rel, dw_cos)

@@ -309,6 +309,13 @@ def test_brute_force_equals_blas(shift, reduction):
     np.testing.assert_allclose(lse, f["lse"], rtol=1e-14)
     np.testing.assert_allclose(dX, a, rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(dW, b, rtol=1e-12, atol=1e-15)
+    # the one-pass form used at full size, against the loops directly
+    fb = oracle.forward_backward(X, W, labels, grad_loss=1.3, row_block=3, **kw)
+    assert fb["n_valid"] == n
+    assert fb["loss"] == pytest.approx(loss, rel=1e-13)
+    np.testing.assert_allclose(fb["lse"], lse, rtol=1e-14)
+    np.testing.assert_allclose(fb["dX"], dX, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(fb["dW"], dW, rtol=1e-12, atol=1e-15)
 
 
 @pytest.mark.parametrize("reduction", ["mean", "sum"])
@@ -352,6 +359,25 @@ def test_out_of_range_targets_are_flagged_and_ignored():
     # an ignore_index inside [0, V) wins over being a class id
     t, valid, n, oor = oracle.effective_targets(np.array([3, 4, 3]), V, ignore_index=3)
     assert valid.tolist() == [False, True, False] and not oor.any()
+
+
+@pytest.mark.parametrize("row_block", [1, 7, 64, 4096])
+def test_one_pass_equals_forward_and_backward(row_block):
+    """forward_backward (one pass, used for whole-matrix checks at full size)
+    is forward() + backward() whatever the row blocking, ragged last block
+    included."""
+    B, S, H, V = 3, 41, 10, 131
+    X, W, labels = _rand(B * S, H, V, 18)
+    for kw in (dict(seq_len=S, shift=True, reduction="mean"), dict(reduction="sum")):
+        f = oracle.forward(X, W, labels, **kw)
+        dX, dW = oracle.backward(X, W, labels, grad_loss=0.7, **kw)
+        fb = oracle.forward_backward(X, W, labels, grad_loss=0.7, row_block=row_block, **kw)
+        assert fb["n_valid"] == f["n_valid"]
+        assert fb["loss"] == pytest.approx(f["loss"], rel=1e-13)
+        np.testing.assert_allclose(fb["lse"], f["lse"], rtol=1e-14)
+        np.testing.assert_array_equal(fb["valid"], f["valid"])
+        np.testing.assert_allclose(fb["dX"], dX, rtol=1e-12, atol=1e-16)
+        np.testing.assert_allclose(fb["dW"], dW, rtol=1e-11, atol=1e-16)
 
 
 def test_sampled_helpers_equal_full():
