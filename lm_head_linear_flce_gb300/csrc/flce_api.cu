@@ -283,6 +283,8 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   off = align_up(off + static_cast<size_t>(p->m_tiles) * 4);
   p->off_active = off;  // active tiles, ascending, then their count
   off = align_up(off + static_cast<size_t>(p->m_tiles + 1) * 4);
+  p->off_done = off;  // per launch and local row tile: R-tile epilogue warps done
+  off = align_up(off + static_cast<size_t>(p->n_blocks * p->v_blocks) * (p->Nb / kPairM) * 4);
   p->off_dxf = off;
   if (p->v_blocks > 1) off = align_up(off + static_cast<size_t>(N) * H * 4);
   p->off_dwf = off;
@@ -458,6 +460,10 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   const bool dw_final = !p.multi_n;
   const bool band = dW && !dw_final;  // bf16 dW over several token blocks: FP32 band
   FLCE_CUDA(cudaMemsetAsync(counters, 0, static_cast<size_t>(p.launches) * 4, s));
+  int* row_done = reinterpret_cast<int*>(ws + p.off_done);
+  const int tiles_per_block = static_cast<int>(p.Nb / kPairM);
+  FLCE_CUDA(cudaMemsetAsync(row_done, 0,
+                            static_cast<size_t>(p.n_blocks * p.v_blocks) * tiles_per_block * 4, s));
   if (dX && !dx_final) FLCE_CUDA(cudaMemsetAsync(dxf, 0, static_cast<size_t>(N) * H * 4, s));
   // rows of skipped tiles are never written by the dX tiles: start from zero
   if (dX && dx_final) FLCE_CUDA(cudaMemsetAsync(dX, 0, static_cast<size_t>(N) * H * 2, s));
@@ -502,7 +508,6 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   // covers active tiles [nb * Nb/256, (nb + 1) * Nb/256); with tiles skipped the
   // last blocks hold fewer tiles or none (the kernels read the active count).
   const int nblk = p.n_blocks * p.v_blocks;
-  const int tiles_per_block = static_cast<int>(p.Nb / kPairM);
   auto block = [&](int b) {
     BlockDesc d;
     const int vb = b / p.n_blocks, nb = b % p.n_blocks;
@@ -555,9 +560,17 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   base.reduction = red;
   base.err = err;
   base.wait_limit_ns = g_wait_limit_ns.load();
+  // X tiles of a row tile are handed out `x_lag` row tiles after its R tiles:
+  // about two tiles per CTA pair are in flight (one in the MMA, the next
+  // being loaded), so by then the R tiles of the row tile have finished.
+  {
+    const int vt = static_cast<int>(cdiv(std::min<int64_t>(p.Vb, V), kBN));
+    const int per_row = vt + (want_dx ? p.h_tiles : 0);
+    base.x_lag = static_cast<int>(cdiv(2 * (dev.sms / 2), per_row)) + 1;
+  }
 
-  // Launch p: recompute dZ block p (R tiles) while block p-1 is contracted
-  // into dX (X tiles) and dW (W tiles).
+  // Launch p: recompute dZ block p (R tiles) and contract it into dX (X tiles)
+  // as its row tiles complete, while block p-1 is contracted into dW (W tiles).
   NvtxRange gemm_range("backward GEMM launches");
   for (int lp = 0; lp <= nblk; ++lp) {
     BwdArgs a = base;
@@ -565,19 +578,20 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
     int tiles = 0;  // at most this many tiles (fewer when token tiles are skipped)
     if (lp < nblk) {
       a.r = block(lp);
+      a.row_done = row_done + static_cast<size_t>(lp) * tiles_per_block;
       tiles += a.r.mt * a.r.vt;
+      if (want_dx) tiles += a.r.mt * p.h_tiles;
     }
-    int xw_vb = -1, xw_nb = -1;
+    int w_vb = -1, w_nb = -1;
     bool overlap = lp >= 1;  // directly after the previous backward launch
     if (lp >= 1) {
       const int b = lp - 1;
-      a.xw = block(b);
-      xw_vb = b / p.n_blocks;
-      xw_nb = b % p.n_blocks;
-      if (want_dw) tiles += a.xw.vt * p.h_tiles;
-      if (want_dx) tiles += a.xw.mt * p.h_tiles;
-      if (band && xw_nb == 0) {
-        FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.xw.vt) * kBN * H * 4, s));
+      a.w = block(b);
+      w_vb = b / p.n_blocks;
+      w_nb = b % p.n_blocks;
+      if (want_dw) tiles += a.w.vt * p.h_tiles;
+      if (band && w_nb == 0) {
+        FLCE_CUDA(cudaMemsetAsync(dwf, 0, static_cast<size_t>(a.w.vt) * kBN * H * 4, s));
         overlap = false;
       }
     }
@@ -585,8 +599,8 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
       overlap = false;  // a band downcast sits between this launch and the previous one
     if (lp == 0) prof_begin(s);
     FLCE_CUDA(launch_bwd_gemm(maps, a, tiles, overlap, s));
-    if (band && lp >= 1 && xw_nb == p.n_blocks - 1) {
-      const int64_t col0 = int64_t{xw_vb} * p.Vb;
+    if (band && lp >= 1 && w_nb == p.n_blocks - 1) {
+      const int64_t col0 = int64_t{w_vb} * p.Vb;
       const int64_t vext = std::min<int64_t>(p.Vb, V - col0);
       FLCE_CUDA(launch_downcast(dwf, static_cast<__nv_bfloat16*>(dW) + col0 * H,
                                 static_cast<size_t>(vext) * H, grad_loss, nv, red, s));

@@ -173,6 +173,46 @@ __device__ __forceinline__ bool wait_parity_cluster(uint32_t bar, uint32_t parit
   return wait_parity_cluster_slow(bar, parity, w);
 }
 
+// ------------------------------------------ counters between CTAs of a grid
+// Orders this thread's accesses of global memory through the async proxy
+// (TMA loads and stores) with its generic-proxy accesses, both ways.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *p >= target (another CTA's release-add), then order the
+// caller's later TMA loads after what that CTA published.  Bounded like
+// wait_parity: false (timeout recorded, abort raised) if the limit runs out or
+// another warp of this CTA aborted.
+static __device__ __noinline__ bool wait_counter_geq(const int* p, int target, const WaitCtx& w) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_gpu(p) >= target) {
+      fence_proxy_async_global();
+      return true;
+    }
+    __nanosleep(64);
+    if ((it & 15u) == 15u) {
+      if (*w.abort) return false;
+      if (global_timer_ns() - t0 > w.limit_ns || it > 0x7ffffff0u) {
+        *w.abort = 1u;
+        raise_error(w.err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

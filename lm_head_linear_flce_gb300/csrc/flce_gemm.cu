@@ -593,21 +593,23 @@ struct Tile {
 // Tiles of this launch, from the number of active token tiles (written on the
 // device before the first backward launch).
 struct Counts {
-  int mt_r, mt_xw;  // active token tiles of the R block and of the XW block
-  int r_tiles, w_tiles, x_tiles, total;
+  int mt_r, mt_w;  // active token tiles of the R block and of the W block
+  int r_tiles, x_tiles, w_tiles, total;
+  int lag;         // X tiles of row tile m follow the R tiles of row tile m + lag
 };
 
 __device__ __forceinline__ Counts tile_counts(const BwdArgs& a) {
   const int n = *a.n_active;
   Counts c;
   c.mt_r = max(0, min(a.r.mt, n - a.r.tile0));
-  c.mt_xw = max(0, min(a.xw.mt, n - a.xw.tile0));
+  c.mt_w = max(0, min(a.w.mt, n - a.w.tile0));
   c.r_tiles = c.mt_r * a.r.vt;
+  c.x_tiles = a.want_dx ? c.mt_r * a.h_tiles : 0;
   // with no active token tile a bf16 dW written directly still needs its zeros:
   // those W tiles run with K = 0 and store 0
-  c.w_tiles = (a.want_dw && (c.mt_xw > 0 || a.dw_final)) ? a.xw.vt * a.h_tiles : 0;
-  c.x_tiles = a.want_dx ? c.mt_xw * a.h_tiles : 0;
-  c.total = c.w_tiles + c.r_tiles + c.x_tiles;
+  c.w_tiles = (a.want_dw && (c.mt_w > 0 || a.dw_final)) ? a.w.vt * a.h_tiles : 0;
+  c.total = c.r_tiles + c.x_tiles + c.w_tiles;
+  c.lag = min(a.x_lag, c.mt_r);
   return c;
 }
 
@@ -616,28 +618,45 @@ __device__ __forceinline__ int token_row(const BwdArgs& a, int tile0, int l) {
   return a.active[tile0 + (l >> 8)] * kPairM + (l & (kPairM - 1));
 }
 
-// Ticket order: R tiles of the R block, then W tiles of the XW block, then X
-// tiles of the XW block.  R tiles come first because only their mainloops may
-// run while the previous launch drains (the other kinds read the dZ slot it
-// writes); the launch ends on the shorter X tiles.  Within a kind the pairs
-// running at once share the larger operand: R tiles vocab-fastest (they share
-// X rows, 59 MB in all, and sweep the 29 MB W block), W tiles H-fastest (they
-// share dZ columns), X tiles H-fastest (they share dZ rows).
+// Ticket order.  The R tiles of the block go row tile by row tile (vocab
+// fastest: the pairs running at once share X rows and sweep the W block), and
+// the X tiles of row tile m are handed out right after the R tiles of row tile
+// m + lag (H-fastest: they share those dZ rows), so they read dZ rows and W
+// block rows that were written or read moments before and are still in L2;
+// an X tile waits (row_done) until every R tile of its row tile has stored.
+// The launch ends on the W tiles of the previous block, complete before the
+// launch began.  R tiles come first because only their mainloops may run
+// while the previous launch drains (their dZ stores wait for it: the slot they
+// write was last read there).
 // m0: local row of the tile (dZ row for R/X tiles, vocab row for W tiles).
+__device__ __forceinline__ Tile tile_r(const BwdArgs& a, int m, int v) {
+  return {kKindR, m * kPairM, v * kBN, a.kb_h};
+}
+__device__ __forceinline__ Tile tile_x(const BwdArgs& a, int m, int h) {
+  return {kKindX, m * kPairM, h * kBN, a.r.vt * (kBN / kBK)};
+}
+
 __device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, const Counts& c, int t) {
-  if (t < c.r_tiles) {
-    const int v = t % a.r.vt, m = t / a.r.vt;
-    return {kKindR, m * kPairM, v * kBN, a.kb_h};
+  const int vt = a.r.vt, ht = a.h_tiles;
+  const int xt = a.want_dx ? ht : 0;  // X tiles per row tile
+  // row tiles 0 .. lag-1: R tiles only
+  const int n_head = c.lag * vt;
+  if (t < n_head) return tile_r(a, t / vt, t % vt);
+  t -= n_head;
+  // row tiles lag .. mt_r-1: R tiles of row tile g + lag, then X tiles of g
+  const int n_mid = (c.mt_r - c.lag) * (vt + xt);
+  if (t < n_mid) {
+    const int g = t / (vt + xt), j = t % (vt + xt);
+    return j < vt ? tile_r(a, g + c.lag, j) : tile_x(a, g, j - vt);
   }
-  t -= c.r_tiles;
-  if (t < c.w_tiles) {
-    const int h = t % a.h_tiles, v = t / a.h_tiles;
-    return {kKindW, v * kPairM, h * kBN, c.mt_xw * (kPairM / kBK)};
-  }
-  t -= c.w_tiles;
-  // dX tiles H-fastest: the pairs running at once share few dZ row blocks
-  const int h = t % a.h_tiles, m = t / a.h_tiles;
-  return {kKindX, m * kPairM, h * kBN, a.xw.vt * (kBN / kBK)};
+  t -= n_mid;
+  // the X tiles of the last `lag` row tiles
+  const int n_tail = c.lag * xt;
+  if (t < n_tail) return tile_x(a, c.mt_r - c.lag + t / xt, t % xt);
+  t -= n_tail;
+  // W tiles of the previous block, H-fastest (they share dZ columns)
+  const int h = t % ht, v = t / ht;
+  return {kKindW, v * kPairM, h * kBN, c.mt_w * (kPairM / kBK)};
 }
 
 }  // namespace
@@ -665,8 +684,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t issued = 0;
       bool prior_done = false;  // the preceding grid (which wrote this dZ slot) has completed
       const uint64_t keep = l2_policy_evict_last();
-      const CUtensorMap* dz_k = &maps.dz_k[a.xw.slot & 1];
-      const CUtensorMap* dz_mn3 = &maps.dz_mn3[a.xw.slot & 1];
+      const CUtensorMap* dz_k = &maps.dz_k[a.r.slot & 1];    // X tiles: this launch's block
+      const CUtensorMap* dz_mn3 = &maps.dz_mn3[a.w.slot & 1];  // W tiles: the previous block
       const bool mn3d = a.mn3d != 0;
       for (;;) {
         int t;
@@ -687,10 +706,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         ring.advance<kTicketRing>();
         if (t >= total) break;
         const Tile tile = decode_ticket(a, cnt, t);
-        if (tile.kind != kKindR && !prior_done) {
-          griddep_wait();
+        if (tile.kind == kKindW && !prior_done) {
+          griddep_wait();  // the W tiles read the dZ slot the previous launch wrote
           prior_done = true;
         }
+        // an X tile reads the dZ rows of its row tile, stored by this launch's
+        // R tiles: wait until all 8 * vt epilogue warps of them have finished
+        if (tile.kind == kKindX &&
+            !wait_counter_geq(a.row_done + (tile.m0 >> 8), 8 * a.r.vt, w))
+          break;
         const int arow = tile.m0 + kBM * rank;     // this CTA's A rows (M)
         const int bcol = tile.n0 + kHalfN * rank;  // this CTA's B columns (N)
         bool ok = true;
@@ -707,11 +731,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             load_xw(&maps.x_k, &maps.w_k, sa, sb, k, token_row(a, a.r.tile0, arow),
                     a.r.col0 + bcol, full_c, keep);
           else if (tile.kind == kKindX)
-            load_dx(dz_k, &maps.w_mn, &maps.w_mn3, mn3d, sa, sb, k, arow, bcol, a.xw.col0,
+            load_dx(dz_k, &maps.w_mn, &maps.w_mn3, mn3d, sa, sb, k, arow, bcol, a.r.col0,
                     full_c);
           else
             load_dw(&maps.x_mn, dz_mn3, &maps.x_mn3, mn3d, sa, sb, k, arow, bcol,
-                    token_row(a, a.xw.tile0, k), full_c, keep);
+                    token_row(a, a.w.tile0, k), full_c, keep);
           issued |= 1u << pipe.idx;
           pipe.advance<kStages>();
         }
@@ -786,8 +810,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (tile.kind == kKindR) {
         epi_dz_staged(tbase, a.r.col0 + tile.n0, a.V, tgt, lse2, st, lane,
                       &maps.dz_st[a.r.slot & 1], tile.n0, y0);
+        // publish: this warp's dZ rows of the tile are in global memory
+        if (lane == 0) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+          red_release_gpu_add(a.row_done + (tile.m0 >> 8), 1);
+        }
+        __syncwarp();
       } else if (tile.kind == kKindX) {
-        const int row = token_row(a, a.xw.tile0, y0);
+        const int row = token_row(a, a.r.tile0, y0);
         if (a.dx_final)
           epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dx_out, row);
         else
@@ -797,12 +828,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                             &maps.dx_out, row);
       } else {
         if (a.dw_final)
-          epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dw_out, a.xw.col0 + y0,
+          epi_final_staged(tbase, tile.n0, a.H, scale, st, lane, &maps.dw_out, a.w.col0 + y0,
                            tile.k_blocks == 0);
         else
           // an FP32 band (scaled later), or the caller's FP32 gradient (scaled here)
           epi_reduce_staged(tbase, tile.n0, a.H, a.dw_accumulate ? scale : 1.f, st, lane,
-                            &maps.dw_out, a.dw_accumulate ? a.xw.col0 + y0 : y0);
+                            &maps.dw_out, a.dw_accumulate ? a.w.col0 + y0 : y0);
       }
       tc_fence_before();
       __syncwarp();
@@ -813,6 +844,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
+  // No CTA exits before the previous launch has completed, so that the
+  // completion of this launch implies the completion of every earlier one.
+  if (threadIdx.x == 0) griddep_wait();
   pair_teardown(tmem, warp);
 }
 

@@ -101,9 +101,16 @@ struct BwdMaps {
                          // dW [V][H] bf16 box 64 x 32 (store) when written directly
 };
 
-// One backward launch: R tiles of block `r`, W and X tiles of block `xw`.
+// One backward launch: the R tiles of block `r`, the X tiles of the same block
+// (each X tile starts once the R tiles of its 256-row token tile have stored
+// their dZ, counted in `row_done`), and the W tiles of block `w` (the previous
+// block, complete when the launch starts).
 struct BwdArgs {
-  BlockDesc r, xw;
+  BlockDesc r, w;
+  int* row_done;   // per local 256-row tile of block r: dZ stores finished, one
+                   // count per epilogue warp (8 per R tile; 8 * r.vt when complete)
+  int x_lag;       // X tiles of a row tile are handed out this many row tiles
+                   // after its R tiles
   int want_dx, want_dw;  // which contractions run (dX tiles, dW tiles)
   int h_tiles;           // 256-column tiles of H
   const int* active;     // active 256-row token tiles, ascending
@@ -142,7 +149,7 @@ struct Plan {
   bool multi_n;           // more than one token block: dW needs an FP32 band
   int launches;           // backward GEMM launches (one per dZ block, plus one)
   size_t off_err, off_t, off_zt, off_part, off_lossp, off_fcnt, off_cnt, off_flags, off_active,
-      off_dxf, off_dwf, off_dz;
+      off_done, off_dxf, off_dwf, off_dz;
   size_t total;
 };
 
