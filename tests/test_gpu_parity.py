@@ -273,3 +273,19 @@ def test_two_token_sequences_with_shift():
     X, W, labels = workloads.random_case(512, 64, 800, seed=79, ignore_frac=0.0)
     got, ref = check_against_oracle(X, W, labels, seq_len=2, shift=True)
     assert got["n_valid"] == 256
+
+
+@pytest.mark.parametrize("need_dW", [True, False])
+def test_dx_tiles_follow_their_row_tiles(need_dW):
+    """The dX tiles of a 256-row tile start as soon as the recompute tiles of
+    that row tile have stored their dZ, interleaved with later recompute tiles:
+    16 row tiles per block (more than the hand-out lag of 11 at H = 2048 and
+    2048-column vocab blocks), three vocab blocks with a ragged last one, and
+    fully ignored row tiles between active ones."""
+    N, H, V, S = 4096, 2048, 6000, 1024
+    flce.flce_set_backward_block(N, N * 2048)
+    X, W, labels = workloads.random_case(N, H, V, seed=31, w_std=0.03)
+    labels[512:1024] = -100   # row tiles 2 and 3 (row 1023 ends a sequence)
+    labels[2560:2817] = -100  # row tile 10: rows 2560-2815 score labels 2561-2816
+    check_against_oracle(X, W, labels, seq_len=S, shift=True, reduction="mean", grad=1.3,
+                         need_dW=need_dW)
