@@ -289,8 +289,9 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   if (p->v_blocks > 1) off = align_up(off + static_cast<size_t>(N) * H * 4);
   p->off_dwf = off;
   if (p->multi_n) off = align_up(off + static_cast<size_t>(p->Vb) * H * 4);
-  // two slots: block p is formed while block p-1 is consumed.  Rows are padded
-  // by 64 elements so that the row pitch is not a power of two.
+  // two slots: block p is formed (and its dX part taken) while the dW part of
+  // block p-1 is consumed.  Rows are padded by 64 elements so that the row
+  // pitch is not a power of two.
   p->dz_ld = p->Vb + 64;
   p->off_dz = off;
   off = align_up(off + 2 * static_cast<size_t>(p->Nb) * p->dz_ld * 2);

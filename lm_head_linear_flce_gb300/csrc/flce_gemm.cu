@@ -23,12 +23,14 @@
 //                    before writing a partial), handed out by a global ticket
 //                    that the leader's producer writes into both CTAs' rings;
 //                    the logits-only variant deals units round robin.
-//   flce_bwd_kernel  backward; one launch holds the R tiles of dZ block p and
-//                    the W and X tiles of block p-1 (two dZ slots, so the
-//                    tiles of one launch never depend on each other).  Tiles
-//                    are handed out by a global atomic ticket in the order R,
-//                    W, X (see decode_ticket); the leader's producer takes
-//                    each ticket and writes it into both CTAs' ticket rings.
+//   flce_bwd_kernel  backward; one launch holds the R and X tiles of dZ block
+//                    p and the W tiles of block p-1 (two dZ slots).  Tiles
+//                    are handed out by a global atomic ticket row tile by row
+//                    tile (see decode_ticket): the X tiles of a 256-row tile
+//                    follow its R tiles and wait for their dZ stores through
+//                    a per-row-tile counter; the W tiles come last.  The
+//                    leader's producer takes each ticket and writes it into
+//                    both CTAs' ticket rings.
 //
 // CTA layout (192 threads, one CTA per SM, persistent):
 //   warp 0      TMA producer: 6-stage ring of (A 128x64, B 128x64) bf16 halves,
@@ -799,6 +801,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (!wait_parity(s.tfull + 8 * accr.idx, accr.phase, w)) break;
+      // before the first store or reduce-add: the previous launch has finished
+      // reading the dZ slot the R tiles write, and its dX / dW additions come
+      // first (a fixed order of FP32 additions)
       if (!prior_done) {
         griddep_wait();
         prior_done = true;
