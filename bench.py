@@ -444,7 +444,7 @@ def cpu_baseline(wl, X, W, L, rows: int):
 
 
 # ------------------------------------------------- the other rows of the path
-ROWS = ("main", "dx_only", "accumulate", "logits", "vocab_shard4")
+ROWS = ("main", "dx_only", "accumulate", "logits", "vocab_shard4", "phases")
 
 
 def run_row(args, world, rank, local):
@@ -544,6 +544,80 @@ def run_row(args, world, rank, local):
             "gpu_launches": launches}), flush=True)
 
 
+def run_phases(args, world, rank, local):
+    """Steady state of each kernel alone: the forward looped for --seconds, then
+    the backward, then a cuBLAS bf16 8192^3 GEMM (torch.matmul, the pool's
+    measured-peak method) as the reference, twice each, with the SM clock and
+    board power sampled during each loop.  At the board's power limit this
+    compares the kernels with cuBLAS on the same GPU at the same moment."""
+    import lm_head_linear_flce_gb300 as flce
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = workloads.get(args.workload)
+    N, H, V = wl.N, wl.H, wl.V
+    X, W, L = (t.to(dev) for t in workloads.make_inputs(wl))
+    kw = dict(seq_len=wl.S, shift=wl.shift, reduction=wl.reduction)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+    ws = torch.empty(flce.workspace_size(N, H, V), dtype=torch.uint8, device=dev)
+    dX, dW = torch.empty_like(X), torch.empty_like(W)
+    _, lse, nv, _ = flce.flce_forward(X, W, L, workspace=ws, **kw)
+    lse, nv = lse.clone(), nv.clone()
+    A = torch.randn(8192, 8192, device=dev).to(torch.bfloat16)
+    B = torch.randn(8192, 8192, device=dev).to(torch.bfloat16)
+    C = torch.empty(8192, 8192, device=dev, dtype=torch.bfloat16)
+    phases = {
+        "forward": (lambda: flce.flce_forward(X, W, L, workspace=ws, **kw), 2 * N * H * V),
+        "backward": (lambda: flce.flce_backward(X, W, L, lse, nv, g, workspace=ws, dX=dX, dW=dW,
+                                                **kw), 6 * N * H * V),
+        "cublas_bf16_gemm": (lambda: torch.matmul(A, B, out=C), 2 * 8192 ** 3),
+    }
+    for fn, _ in phases.values():
+        for _ in range(args.warmup):
+            fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for rnd in range(2):
+        for name, (fn, flops) in phases.items():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            n = max(3, int(args.seconds * 1e3 / e0.elapsed_time(e1)))
+            clocks = ClockSampler(local)
+            clocks.start()
+            time.sleep(0.3)
+            h0 = time.time()
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            h1 = time.time()
+            # the second half of the loop (after the power controller settled)
+            clocks.window(0.5 * (h0 + h1), h1)
+            clk = clocks.stop()
+            ms = e0.elapsed_time(e1) / n
+            tfl = flops / (ms / 1e3) / 1e12
+            rec = {"ms": round(ms, 4), "tflops": round(tfl, 1), "clocks": clk}
+            if clk and clk.get("sm_mhz"):
+                sms = torch.cuda.get_device_properties(dev).multi_processor_count
+                rec["per_clock"] = round(tfl * 1e12 / (sms * BF16_FLOP_PER_CLK_PER_SM *
+                                                       clk["sm_mhz"] * 1e6), 4)
+                rec["watts_per_tflops"] = round(clk["power_w"] / tfl, 4)
+            out.setdefault(name, []).append(rec)
+    best = {k: max(v, key=lambda r: r["tflops"]) for k, v in out.items()}
+    ref = best["cublas_bf16_gemm"]["tflops"]
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "row": "phases", "unit": "TFLOP/s", "workload": wl.name,
+            "seconds_per_loop": args.seconds, "phases": out,
+            "vs_cublas_same_run": {k: round(v["tflops"] / ref, 4) for k, v in best.items()},
+            "dtype": "bf16", "data": "synthetic"}), flush=True)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -586,9 +660,12 @@ def main(argv=None):
     p.add_argument("--ref-rows", type=int, default=8)
     p.add_argument("--tokens", type=int, default=0, help="override N (profiling cases)")
     p.add_argument("--vocab", type=int, default=0, help="override V (profiling cases)")
+    p.add_argument("--seconds", type=float, default=3.0,
+                   help="--row phases: length of each kernel's steady-state loop")
     p.add_argument("--row", default="main", choices=ROWS,
-                   help="main: the fused forward + backward step; the others time the path's "
-                        "other entry points")
+                   help="main: the fused forward + backward step; phases: each kernel's "
+                        "steady state beside a cuBLAS GEMM; the others time the path's other "
+                        "entry points")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
@@ -596,6 +673,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.row == "phases":
+            run_phases(args, world, rank, local)
         elif args.row != "main":
             run_row(args, world, rank, local)
         else:

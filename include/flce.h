@@ -266,7 +266,9 @@ void flce_set_wait_limit_ns(int64_t limit_ns);
  * A value <= 0 leaves that cap automatic: at most 32 Mi elements (a 64 MB
  * block) when N <= 8192 and 64 Mi (128 MB) above, and every token row in one
  * block while that leaves at least 2048 vocab columns per block (so dW is
- * written once, with no FP32 accumulator across token blocks).  Smaller
+ * written once, with no FP32 accumulator across token blocks); above 8192
+ * rows, with every row in one block, the cap doubles (up to 128 Mi elements,
+ * 256 MB) while a block would hold fewer than 76 dW tiles of 256 x 256.  Smaller
  * blocks mean less workspace and more FP32 accumulation traffic.
  * Process-wide; flce_workspace_size and the calls that use the workspace must
  * see the same setting.

@@ -29,6 +29,11 @@ constexpr int64_t kSmallDzBlockElems = int64_t{32} << 20;
 constexpr int64_t kLargeDzBlockElems = int64_t{64} << 20;
 constexpr int64_t kSmallBlockRows = 8192;
 constexpr int64_t kMinBlockCols = 2048;
+// Above kSmallBlockRows rows the block may grow to this many elements (256 MB)
+// so that a launch holds at least kMinWTiles dW tiles (one per CTA pair of a
+// 152-SM GB300): fewer leave pairs idle while the launch's dW tiles finish.
+constexpr int64_t kMaxAutoBlockElems = int64_t{128} << 20;
+constexpr int64_t kMinWTiles = 76;
 constexpr size_t kAlign = 256;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
@@ -253,7 +258,19 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
     p->Nb = cdiv(std::max(p->m_tiles, 1), nblk) * kPairM;
   }
   const int64_t v_pad = int64_t{p->v_tiles} * kBN;
-  p->Vb = std::min<int64_t>(v_pad, std::max<int64_t>(kBN, max_elems / p->Nb / kBN * kBN));
+  auto cols = [&](int64_t elems) {
+    return std::min<int64_t>(v_pad, std::max<int64_t>(kBN, elems / p->Nb / kBN * kBN));
+  };
+  p->Vb = cols(max_elems);
+  // large problems (every row in one block): grow the block while its dW tiles
+  // would leave CTA pairs without one
+  if (g_block_elems.load() <= 0 && n_pad > kSmallBlockRows && p->Nb == n_pad) {
+    while ((p->Vb / kBN) * p->h_tiles < kMinWTiles && max_elems < kMaxAutoBlockElems &&
+           p->Vb < v_pad) {
+      max_elems *= 2;
+      p->Vb = cols(max_elems);
+    }
+  }
   p->n_blocks = N > 0 ? static_cast<int>(cdiv(N, p->Nb)) : 0;
   p->v_blocks = static_cast<int>(cdiv(V, p->Vb));
   p->multi_n = p->n_blocks > 1;
@@ -383,6 +400,7 @@ flce_status forward_impl(const void* X, const void* W, const int64_t* labels, in
   a.tiles_n = p.v_tiles;
   a.group = p.fwd_group;
   a.units = p.m_tiles * p.v_units;
+  a.band = forward_band_tiles(p.m_tiles, H);
   a.k_blocks = static_cast<int>(cdiv(H, kBK));
   a.N = static_cast<int>(N);
   a.H = static_cast<int>(H);
@@ -780,6 +798,7 @@ flce_status flce_logits(const void* X, const void* W, int64_t N, int64_t H, int6
   a.tiles_n = static_cast<int>(cdiv(V, kBN));
   a.group = kFwdGroup;
   a.units = a.tiles_m * static_cast<int>(cdiv(a.tiles_n, kFwdGroup));
+  a.band = a.tiles_m;  // units dealt round robin, vocab group by vocab group
   a.k_blocks = static_cast<int>(cdiv(H, kBK));
   a.N = static_cast<int>(N);
   a.H = static_cast<int>(H);

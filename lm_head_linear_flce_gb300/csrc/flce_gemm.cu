@@ -431,6 +431,24 @@ __device__ void drain_mma(const Smem& s, const WaitCtx& w0) {
 // their progress drifts apart.  The logits path, which has no workspace for a
 // ticket counter, deals units round robin instead.
 
+// Row tile and vocab group of unit u: bands of a.band row tiles (the last one
+// may be shorter), vocab group by vocab group within a band, row tile fastest.
+struct Unit {
+  int m, vg;
+};
+__device__ __forceinline__ Unit unit_of(const GemmArgs& a, int u) {
+  const int vgroups = (a.tiles_n + a.group - 1) / a.group;
+  const int full = a.tiles_m / a.band;              // bands of a.band row tiles
+  const int in_full = full * a.band * vgroups;
+  if (u < in_full) {
+    const int b = u / (a.band * vgroups), r = u % (a.band * vgroups);
+    return {b * a.band + r % a.band, r / a.band};
+  }
+  const int last = a.tiles_m - full * a.band;       // > 0 here
+  const int r = u - in_full;
+  return {full * a.band + r % last, r / last};
+}
+
 // Next unit for a role.  `leader_producer` takes tickets; the other roles read
 // them from this CTA's ring.  Returns false if aborted.
 template <bool DYN>
@@ -503,9 +521,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       while (ok && next_unit<kDyn>(a, s, ring, u, leader, !leader, true, lane, false, w) &&
              u < a.units) {
-        const int arow = (u % a.tiles_m) * kPairM + kBM * rank;
+        const Unit un = unit_of(a, u);
+        const int arow = un.m * kPairM + kBM * rank;
         for (int g = 0; g < a.group && ok; ++g) {
-          const int nt = (u / a.tiles_m) * a.group + g;
+          const int nt = un.vg * a.group + g;
           if (nt >= a.tiles_n) break;
           const int brow = nt * kBN + kHalfN * rank;
           for (int kb = 0; kb < a.k_blocks; ++kb) {
@@ -530,8 +549,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       while (ok && next_unit<kDyn>(a, s, ring, u, false, false, false, lane, false, w) &&
              u < a.units) {
+        const Unit un = unit_of(a, u);
         for (int g = 0; g < a.group; ++g) {
-          const int nt = (u / a.tiles_m) * a.group + g;
+          const int nt = un.vg * a.group + g;
           if (nt >= a.tiles_n) break;
           ok = wait_parity_cluster(s.tempty + 8 * accr.idx, accr.phase ^ 1u, w);
           if (!ok) break;
@@ -554,11 +574,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     while (ok && next_unit<kDyn>(a, s, ring, u, false, false, true, lane, true, w) &&
            u < a.units) {
-      const int row = (u % a.tiles_m) * kPairM + r;
+      const Unit un = unit_of(a, u);
+      const int row = un.m * kPairM + r;
       const int t = (MODE == kFwdLse && row < a.N) ? a.targets[row] : -1;
       float run_m = -INFINITY, run_s = 0.f;
       for (int g = 0; g < a.group; ++g) {
-        const int nt = (u / a.tiles_m) * a.group + g;
+        const int nt = un.vg * a.group + g;
         if (nt >= a.tiles_n) break;
         ok = wait_parity(s.tfull + 8 * accr.idx, accr.phase, w);
         if (!ok) break;
@@ -575,7 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         accr.advance<kNumAcc>();
       }
       if (MODE == kFwdLse && ok && row < a.N)
-        a.partials[static_cast<size_t>(u / a.tiles_m) * a.N + row] = make_float2(run_m, run_s);
+        a.partials[static_cast<size_t>(un.vg) * a.N + row] = make_float2(run_m, run_s);
     }
     if (MODE == kFwdLogits) {
       if (lane == 0) bulk_wait_all();

@@ -58,6 +58,8 @@ enum GemmKind : int {
 // Forward GEMM launch.
 struct GemmArgs {
   int tiles_m, tiles_n, group, units, k_blocks;
+  int band;  // row tiles per band: units go band by band, vocab group by vocab
+             // group within a band, row tile fastest (a band's X rows stay in L2)
   int N, H, V;
   const int* targets;  // [N]: local column, -1 (no valid target) or kTargetElsewhere
   float2* partials;    // [units_n][N]: per-row (max, sum exp(z - max)) over a work unit
@@ -154,6 +156,18 @@ struct Plan {
 };
 
 bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p);
+
+// Row tiles per band of the forward's unit order: as many as keep the band's
+// X rows (256 * H * 2 bytes per row tile) within kFwdBandBytes, balanced over
+// the bands.  With one band the order is plain vocab group by vocab group.
+constexpr int64_t kFwdBandBytes = int64_t{40} << 20;
+inline int forward_band_tiles(int64_t m_tiles, int64_t H) {
+  const int64_t per_tile = int64_t{256} * H * 2;
+  int64_t cap = kFwdBandBytes / per_tile;
+  if (cap < 1) cap = 1;
+  const int64_t bands = (m_tiles + cap - 1) / cap;
+  return static_cast<int>(bands > 0 ? (m_tiles + bands - 1) / bands : 1);
+}
 
 // Vocab tiles per forward work unit for a vocabulary of v_tiles 256-column
 // tiles: at least kFwdGroup, and few enough units (<= kFwdSplits) per row tile.

@@ -135,6 +135,7 @@ extern "C" flce_status flce_forward_noalloc(const void* X, const void* W, const 
     a.tiles_n = static_cast<int>(v_tiles);
     a.group = group;
     a.units = static_cast<int>(m_tiles * v_units);
+    a.band = forward_band_tiles(m_tiles, H);
     a.k_blocks = static_cast<int>((H + kBK - 1) / kBK);
     a.N = static_cast<int>(N);
     a.H = static_cast<int>(H);
