@@ -798,7 +798,7 @@ flce_status flce_logits(const void* X, const void* W, int64_t N, int64_t H, int6
   a.tiles_n = static_cast<int>(cdiv(V, kBN));
   a.group = kFwdGroup;
   a.units = a.tiles_m * static_cast<int>(cdiv(a.tiles_n, kFwdGroup));
-  a.band = a.tiles_m;  // units dealt round robin, vocab group by vocab group
+  a.band = forward_band_tiles(a.tiles_m, H);  // units dealt round robin, band by band
   a.k_blocks = static_cast<int>(cdiv(H, kBK));
   a.N = static_cast<int>(N);
   a.H = static_cast<int>(H);
