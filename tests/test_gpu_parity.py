@@ -289,3 +289,12 @@ def test_dx_tiles_follow_their_row_tiles(need_dW):
     labels[2560:2817] = -100  # row tile 10: rows 2560-2815 score labels 2561-2816
     check_against_oracle(X, W, labels, seq_len=S, shift=True, reduction="mean", grad=1.3,
                          need_dW=need_dW)
+
+
+def test_forward_row_bands_with_a_ragged_last_band():
+    """The forward hands out its work units band by band (as many 256-row tiles
+    as keep 40 MB of X): at H = 8192 a row tile holds 4 MB of X, so 11 row
+    tiles (the last one ragged) go in bands of 6 and 5."""
+    N, H, V = 2800, 8192, 3000
+    X, W, labels = workloads.random_case(N, H, V, seed=41, x_std=0.5, w_std=0.01)
+    check_against_oracle(X, W, labels, reduction="sum", grad=0.5)
