@@ -619,6 +619,9 @@ struct Counts {
   int mt_r, mt_w;  // active token tiles of the R block and of the W block
   int r_tiles, x_tiles, w_tiles, total;
   int lag;         // X tiles of row tile m follow the R tiles of row tile m + lag
+  int first;       // R tiles handed out before the W tiles when w_early
+  bool w_early;    // W tiles (K = the block's active rows) at least 3x as long as
+                   // R tiles (K = H): hand them out after one wave of R tiles
 };
 
 __device__ __forceinline__ Counts tile_counts(const BwdArgs& a) {
@@ -633,6 +636,8 @@ __device__ __forceinline__ Counts tile_counts(const BwdArgs& a) {
   c.w_tiles = (a.want_dw && (c.mt_w > 0 || a.dw_final)) ? a.w.vt * a.h_tiles : 0;
   c.total = c.r_tiles + c.x_tiles + c.w_tiles;
   c.lag = min(a.x_lag, c.mt_r);
+  c.w_early = c.mt_w * kPairM >= 3 * a.H;
+  c.first = min(c.r_tiles, static_cast<int>(gridDim.x >> 1));
   return c;
 }
 
@@ -659,7 +664,24 @@ __device__ __forceinline__ Tile tile_x(const BwdArgs& a, int m, int h) {
   return {kKindX, m * kPairM, h * kBN, a.r.vt * (kBN / kBK)};
 }
 
+__device__ __forceinline__ Tile decode_rx(const BwdArgs& a, const Counts& c, int t);
+
+// When the W tiles are long (w_early), they are handed out right after the
+// first wave of R tiles (one per CTA pair) instead of last, so that the launch
+// ends on the shorter kinds and the next launch, which waits for this one to
+// end before its first store, is not held up by a tail of long W tiles.
 __device__ __forceinline__ Tile decode_ticket(const BwdArgs& a, const Counts& c, int t) {
+  if (!c.w_early) return decode_rx(a, c, t);
+  if (t < c.first) return decode_rx(a, c, t);
+  if (t < c.first + c.w_tiles) {
+    const int u = t - c.first, ht = a.h_tiles;
+    return {kKindW, (u / ht) * kPairM, (u % ht) * kBN, c.mt_w * (kPairM / kBK)};
+  }
+  return decode_rx(a, c, t - c.w_tiles);
+}
+
+// R and X tiles in their per-row-tile order, then (unless w_early) W tiles.
+__device__ __forceinline__ Tile decode_rx(const BwdArgs& a, const Counts& c, int t) {
   const int vt = a.r.vt, ht = a.h_tiles;
   const int xt = a.want_dx ? ht : 0;  // X tiles per row tile
   // row tiles 0 .. lag-1: R tiles only
