@@ -69,9 +69,11 @@ typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 } flce_reduction;
 /*
  * Bytes of device workspace flce_forward and flce_backward need for these
  * sizes (one buffer serves both; it need not survive from forward to
- * backward).  It is O(N*H + Vb*H + 128*N + tiles), never O(N*V): FP32
- * accumulators for dX and for one vocab band of dW, a bounded bf16 block of
- * dZ, and per-row partial log-sum-exps (at most 128 per row, whatever V is).
+ * backward).  It is O(N*H + Vb*H + Nb*Vb + 128*N + tiles), never O(N*V):
+ * FP32 accumulators for dX and for one vocab band of dW, two bounded bf16
+ * blocks of dZ (Nb x Vb each, at most 2^27 elements; see
+ * flce_set_backward_block), and per-row partial log-sum-exps (at most 128 per
+ * row, whatever V is).
  * Returns 0 for invalid sizes.
  */
 size_t flce_workspace_size(int64_t N, int64_t H, int64_t V);
