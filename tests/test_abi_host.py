@@ -188,3 +188,28 @@ def test_forward_partials_do_not_grow_with_the_vocabulary(lib):
     # vocabulary past 512 tiles the noalloc size limit no longer moves
     assert _noalloc_need(8192, 1 << 22) == _noalloc_need(8192, 1 << 24)
     assert _noalloc_need(8192, 152064) < _noalloc_need(8192, 1 << 22)
+
+
+def test_large_blocks_grow_until_a_launch_holds_enough_dw_tiles(lib):
+    """Above 8192 rows, with every row in one block, the automatic dZ block
+    doubles (up to 2^27 elements) while it would hold fewer than 76 dW tiles of
+    256 x 256 (include/flce.h, flce_set_backward_block): at N = 32768 and
+    H = 2048 a 64 Mi-element block has 2048 vocab columns (8 x 8 = 64 dW
+    tiles), so it grows to 4096 columns: both dZ slots gain 32768 x 2048
+    bf16 elements over the same plan with the cap set to 64 Mi by hand."""
+    N, H, V = 32768, 2048, 151936
+    auto = lib.flce_workspace_size(N, H, V)
+    lib.flce_set_backward_block(0, 64 << 20)
+    try:
+        capped = lib.flce_workspace_size(N, H, V)
+    finally:
+        lib.flce_set_backward_block(0, 0)
+    # (the per-launch counters shrink a little with half as many blocks)
+    assert abs((auto - capped) - 2 * N * 2048 * 2) <= 64 * 1024, auto - capped
+    # enough dW tiles already (H = 4096: 16 x 16 at 4096 columns): no growth
+    lib.flce_set_backward_block(0, 64 << 20)
+    try:
+        capped = lib.flce_workspace_size(16384, 4096, V)
+    finally:
+        lib.flce_set_backward_block(0, 0)
+    assert lib.flce_workspace_size(16384, 4096, V) == capped
