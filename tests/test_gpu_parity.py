@@ -69,6 +69,7 @@ def test_tiny_workload():
     (512, 320, 2304, 256, False, "mean", (128, 128 * 256)),  # smallest blocks, exact tiles
     (1, 64, 7, None, False, "mean", None),               # one row, vocab smaller than a tile
     (130, 72, 257, None, False, "sum", (128, 128 * 256)),  # one column past a tile
+    (2048, 192, 1500, 512, True, "mean", (2048, 2048 * 256)),  # every row, one vocab tile a block
 ])
 def test_odd_shapes(N, H, V, S, shift, red, blocks):
     if blocks:
