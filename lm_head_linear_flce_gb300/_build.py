@@ -2,7 +2,7 @@
 
 Each .cu file is compiled to an object in parallel, then linked with the
 static CUDA runtime (the library needs no libcudart at load time and finds
-the driver entry points it uses at run time).
+the CUDA driver entry points it uses at run time).
 """
 from __future__ import annotations
 

@@ -187,7 +187,7 @@ void note_wait_limit(unsigned long long limit_ns);
 
 // 2-D tensor map over a row-major [outer][inner] matrix (rows `row_bytes`
 // apart) with 128-byte swizzle and the given box; out-of-bounds elements read
-// as zero and are not written.  False if the driver rejects it.
+// as zero and are not written.  False if the CUDA driver rejects it.
 bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);

@@ -89,7 +89,7 @@ def test_peak_extra_memory_is_the_workspace(name):
     assert ws <= peak_alloc - outputs <= ws + 3 * MiB + 4 * 512, (peak_alloc - outputs, ws)
     assert ws <= documented_bound(N, H, V), (ws, documented_bound(N, H, V))
     # nothing outside torch's allocator: free memory moved only by torch's
-    # reserve (up to the driver's own bookkeeping for new mappings)
+    # reserve (up to the CUDA driver's own bookkeeping for new mappings)
     assert abs((free0 - free1) - (reserved1 - reserved0)) <= 8 * MiB, (free0 - free1,
                                                                        reserved1 - reserved0)
     if N * V >= 1 << 30:  # the Qwen-sized workloads: far below the logits
