@@ -270,7 +270,9 @@ void flce_set_wait_limit_ns(int64_t limit_ns);
  * block while that leaves at least 2048 vocab columns per block (so dW is
  * written once, with no FP32 accumulator across token blocks); above 8192
  * rows, with every row in one block, the cap doubles (up to 128 Mi elements,
- * 256 MB) while a block would hold fewer than 76 dW tiles of 256 x 256.  Smaller
+ * 256 MB) while a block would hold fewer than 76 dW tiles of 256 x 256; and
+ * the block's vocab width Vb is then capped so that its W rows (Vb x H bf16)
+ * take at most 64 MiB (a multiple of 256 columns, at least 256).  Smaller
  * blocks mean less workspace and more FP32 accumulation traffic.
  * Process-wide; flce_workspace_size and the calls that use the workspace must
  * see the same setting.

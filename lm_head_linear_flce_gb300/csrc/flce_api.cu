@@ -34,6 +34,10 @@ constexpr int64_t kMinBlockCols = 2048;
 // 152-SM GB300): fewer leave pairs idle while the launch's dW tiles finish.
 constexpr int64_t kMaxAutoBlockElems = int64_t{128} << 20;
 constexpr int64_t kMinWTiles = 76;
+// The block's W rows (Vb x H bf16), which the recompute tiles sweep once per
+// row tile, are kept within this many bytes, about half of L2, so that they
+// are still there for the next row tile (binds only for H >= 4096).
+constexpr int64_t kMaxWBlockBytes = int64_t{64} << 20;
 constexpr size_t kAlign = 256;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
@@ -271,6 +275,8 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
       p->Vb = cols(max_elems);
     }
   }
+  if (g_block_elems.load() <= 0)
+    p->Vb = std::min<int64_t>(p->Vb, std::max<int64_t>(kBN, kMaxWBlockBytes / (2 * H) / kBN * kBN));
   p->n_blocks = N > 0 ? static_cast<int>(cdiv(N, p->Nb)) : 0;
   p->v_blocks = static_cast<int>(cdiv(V, p->Vb));
   p->multi_n = p->n_blocks > 1;

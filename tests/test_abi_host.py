@@ -213,3 +213,28 @@ def test_large_blocks_grow_until_a_launch_holds_enough_dw_tiles(lib):
     finally:
         lib.flce_set_backward_block(0, 0)
     assert lib.flce_workspace_size(16384, 4096, V) == capped
+
+
+def test_w_block_kept_within_64_mib(lib):
+    """The automatic block's vocab width is capped so that its W rows (Vb x H
+    bf16) take at most 64 MiB (include/flce.h, flce_set_backward_block).  At
+    N = 4096 and H = 8192 the 32 Mi-element cap alone gives 8192 columns
+    (128 MiB of W rows), so the width drops to 4096: the plan is the one a
+    16 Mi-element cap set by hand gives, and both dZ slots shrink by 4096 x
+    4096 bf16 elements against the 32 Mi-element cap set by hand (which the
+    W-row cap leaves alone).  At H = 3584 it does not bind."""
+    N, H, V = 4096, 8192, 128256
+    auto = lib.flce_workspace_size(N, H, V)
+    try:
+        lib.flce_set_backward_block(0, 16 << 20)
+        narrow = lib.flce_workspace_size(N, H, V)
+        lib.flce_set_backward_block(0, 32 << 20)
+        wide = lib.flce_workspace_size(N, H, V)
+        lib.flce_set_backward_block(0, 32 << 20)
+        qwen2_by_hand = lib.flce_workspace_size(8192, 3584, 152064)
+    finally:
+        lib.flce_set_backward_block(0, 0)
+    assert auto == narrow
+    # (the per-launch counters grow a little with twice as many blocks)
+    assert abs((wide - auto) - 2 * N * 4096 * 2) <= 64 * 1024, wide - auto
+    assert lib.flce_workspace_size(8192, 3584, 152064) == qwen2_by_hand
