@@ -338,24 +338,15 @@ def run_ours(args, world, rank, local):
 
     peaks, src = load_peaks()
     flops = wl.flops
-    # The backward skips 256-row token tiles without any target; FLOPs actually
-    # executed per step (reported beside the algorithmic 8*N*H*V):
-    tgt = torch.full((N,), -100, dtype=torch.int64)
-    if wl.shift:
-        lab = Lh.view(-1, wl.S)
-        tgt.view(-1, wl.S)[:, :-1] = lab[:, 1:]
-    else:
-        tgt.copy_(Lh)
-    has = (tgt != -100).view(-1)
-    pad = (-N) % 256
-    tiles = torch.cat([has, torch.zeros(pad, dtype=torch.bool)]).view(-1, 256).any(1)
-    active_rows = min(N, int(tiles.sum()) * 256)
+    # FLOPs actually executed per step (reported beside the algorithmic
+    # 8*N*H*V, and the basis of the backward's roofline)
+    active_rows = backward_rows(wl, Lh)
     exec_flops = 2 * N * H * V + 6 * active_rows * H * V
     tflops = flops / (ms_step / 1e3) / 1e12 * 1.0
     tflops_all = world * tflops
     # dominant tensor-core kernel of the step: forward launch (2NHV) or the
-    # backward launches (recompute + dX + dW, 6NHV)
-    kind_flops = {"forward": 2 * N * H * V, "backward": 6 * N * H * V}
+    # backward launches (recompute + dX + dW: 6 x H x V per row they run on)
+    kind_flops = {"forward": 2 * N * H * V, "backward": 6 * active_rows * H * V}
     kinds = {k: v for k, v in prof.items() if v[1] > 0}
     dom = max(kinds, key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
@@ -382,6 +373,8 @@ def run_ours(args, world, rank, local):
         "launches_per_step": dom_n / args.steps,
         "avg_launch_ms": dom_ms / dom_n,
         "flops_per_launch": kind_flops[dom] * args.steps / dom_n,
+        "flops_basis": ("forward: 2*N*H*V; backward: 6*H*V per row it runs on "
+                        f"({active_rows} of N={N}: the rows with a valid target, in 256-row tiles)"),
         "share_of_step": round(dom_ms / (ms_step * args.steps), 4),
         "per_kind_ms_per_step": {k: round(v[0] / args.steps, 3) for k, v in kinds.items()},
         "per_kind_tflops": {k: round(kind_flops[k] * args.steps / (v[0] / 1e3) / 1e12, 1)
@@ -546,6 +539,27 @@ def run_row(args, world, rank, local):
             "gpu_launches": launches}), flush=True)
 
 
+def backward_rows(wl, labels):
+    """Rows the backward runs on: those with a valid target, gathered into dense
+    256-row tiles when V spans several dZ blocks (a backward with dX), else
+    the 256-row token tiles that hold one (include/flce.h, flce_backward)."""
+    import lm_head_linear_flce_gb300 as flce
+    N, H, V = wl.N, wl.H, wl.V
+    tgt = torch.full((N,), -100, dtype=torch.int64)
+    if wl.shift:
+        lab = labels.view(-1, wl.S)
+        tgt.view(-1, wl.S)[:, :-1] = lab[:, 1:]
+    else:
+        tgt.copy_(labels)
+    has = (tgt != -100).view(-1)
+    _, Vb = flce.flce_backward_blocking(N, H, V)
+    if V > Vb:
+        return min(N, -(-int(has.sum()) // 256) * 256)
+    pad = (-N) % 256
+    tiles = torch.cat([has, torch.zeros(pad, dtype=torch.bool)]).view(-1, 256).any(1)
+    return min(N, int(tiles.sum()) * 256)
+
+
 def run_phases(args, world, rank, local):
     """Steady state of each kernel alone: the forward looped for --seconds, then
     the backward, then a cuBLAS bf16 8192^3 GEMM (torch.matmul, the pool's
@@ -571,7 +585,7 @@ def run_phases(args, world, rank, local):
     phases = {
         "forward": (lambda: flce.flce_forward(X, W, L, workspace=ws, **kw), 2 * N * H * V),
         "backward": (lambda: flce.flce_backward(X, W, L, lse, nv, g, workspace=ws, dX=dX, dW=dW,
-                                                **kw), 6 * N * H * V),
+                                                **kw), 6 * backward_rows(wl, L.cpu()) * H * V),
         "cublas_bf16_gemm": (lambda: torch.matmul(A, B, out=C), 2 * 8192 ** 3),
     }
     for fn, _ in phases.values():

@@ -72,8 +72,9 @@ typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 } flce_reduction;
  * backward).  It is O(N*H + Vb*H + Nb*Vb + 128*N + tiles), never O(N*V):
  * FP32 accumulators for dX and for one vocab band of dW, two bounded bf16
  * blocks of dZ (Nb x Vb each, at most 2^27 elements; see
- * flce_set_backward_block), and per-row partial log-sum-exps (at most 128 per
- * row, whatever V is).
+ * flce_set_backward_block), per-row partial log-sum-exps (at most 128 per
+ * row, whatever V is), and 16 bytes per row of targets and of the dense-row
+ * maps of the backward.
  * Returns 0 for invalid sizes.
  */
 size_t flce_workspace_size(int64_t N, int64_t H, int64_t V);
@@ -104,11 +105,19 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels,
  *   lse, n_valid    device, as written by flce_forward for the same inputs.
  *   grad_loss       device float, 1 element: g = d(outer loss)/d(loss).
  *   dX              device bf16 [N, H] or NULL to skip it (e.g. when only W is
- *                   trained); written, not accumulated.
+ *                   trained); written, not accumulated.  It must not overlap
+ *                   X, W, labels or lse (FLCE_ERR_INVALID_ARG): while the call
+ *                   runs it may hold a dense copy of the rows of X that have a
+ *                   valid target.
  *   dW              device bf16 [V, H] or NULL to skip it (a frozen LM head,
  *                   as in LoRA fine-tuning); written, not accumulated.
  * Gradients are accumulated in FP32 and rounded to bf16 (round to nearest even)
  * once, after the scale g / n_valid (mean) or g (sum) is applied in FP32.
+ * Rows without a valid target contribute nothing: with dX requested and V
+ * spanning several dZ blocks, the rows that have one are gathered into dX's
+ * buffer and the contractions run on ceil(rows / 256) dense 256-row tiles (dX
+ * is put back in token order, 0 on the other rows, by the final downcast);
+ * otherwise they run on the 256-row token tiles that hold a valid target.
  * The other arguments have the same meaning as in flce_forward.
  */
 flce_status flce_backward(const void* X, const void* W, const int64_t* labels,
@@ -278,6 +287,14 @@ void flce_set_wait_limit_ns(int64_t limit_ns);
  * see the same setting.
  */
 void flce_set_backward_block(int64_t max_rows, int64_t max_block_elems);
+
+/*
+ * The backward's dZ block for these sizes under the current setting: *Nb
+ * token rows (a multiple of 256) by *Vb vocab columns (a multiple of 256).
+ * V > *Vb means several vocab blocks, and then a backward with dX gathers
+ * the rows that have a valid target (see flce_backward).  Host only.
+ */
+flce_status flce_backward_blocking(int64_t N, int64_t H, int64_t V, int64_t* Nb, int64_t* Vb);
 
 /*
  * Measurement hooks.

@@ -21,7 +21,8 @@ import torch
 __all__ = [
     "FlceError", "library", "library_path", "workspace_size", "flce_forward", "flce_backward",
     "flce_get_error", "flce_selftest_wait_timeout", "flce_set_wait_limit_ns",
-    "flce_set_backward_block", "flce_kernel_launch_count", "flce_last_launch_wait_limit_ns",
+    "flce_set_backward_block", "flce_backward_blocking", "flce_kernel_launch_count",
+    "flce_last_launch_wait_limit_ns",
     "flce_profile_enable",
     "flce_profile_collect", "PROFILE_KINDS", "flce_forward_noalloc", "flce_backward_accumulate",
     "flce_logits", "flce_forward_vocab_shard", "flce_merge_vocab_shards",
@@ -76,6 +77,9 @@ def library() -> ctypes.CDLL:
     lib.flce_set_wait_limit_ns.restype = None
     lib.flce_set_backward_block.argtypes = [c_i64, c_i64]
     lib.flce_set_backward_block.restype = None
+    lib.flce_backward_blocking.argtypes = [c_i64, c_i64, c_i64, ctypes.POINTER(c_i64),
+                                           ctypes.POINTER(c_i64)]
+    lib.flce_backward_blocking.restype = c_int
     lib.flce_kernel_launch_count.argtypes = []
     lib.flce_kernel_launch_count.restype = c_i64
     lib.flce_profile_enable.argtypes = [c_int]
@@ -324,6 +328,14 @@ def flce_set_wait_limit_ns(limit_ns: int) -> None:
 def flce_set_backward_block(max_rows: int = 0, max_block_elems: int = 0) -> None:
     """Caps the backward's dZ block (0 restores the defaults); see include/flce.h."""
     library().flce_set_backward_block(int(max_rows), int(max_block_elems))
+
+
+def flce_backward_blocking(N: int, H: int, V: int) -> tuple[int, int]:
+    """The backward's dZ block (token rows, vocab columns) for these sizes."""
+    nb, vb = ctypes.c_int64(), ctypes.c_int64()
+    _check(library().flce_backward_blocking(int(N), int(H), int(V), ctypes.byref(nb),
+                                            ctypes.byref(vb)), "flce_backward_blocking")
+    return nb.value, vb.value
 
 
 def flce_kernel_launch_count() -> int:

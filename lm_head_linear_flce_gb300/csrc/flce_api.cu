@@ -46,6 +46,12 @@ std::atomic<int64_t> g_block_rows{0};   // 0: automatic
 std::atomic<int64_t> g_block_elems{0};  // 0: automatic
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct DeviceInfo {
@@ -306,6 +312,16 @@ bool make_plan(int64_t N, int64_t H, int64_t V, Plan* p) {
   off = align_up(off + static_cast<size_t>(p->m_tiles) * 4);
   p->off_active = off;  // active tiles, ascending, then their count
   off = align_up(off + static_cast<size_t>(p->m_tiles + 1) * 4);
+  // dense rows (rows with a valid target gathered to the front): per-tile
+  // offsets, and per dense row its target and lse, per token row its dense index
+  p->off_toff = off;
+  off = align_up(off + static_cast<size_t>(p->m_tiles + 1) * 4);
+  p->off_tc = off;
+  off = align_up(off + static_cast<size_t>(N) * 4);
+  p->off_lc = off;
+  off = align_up(off + static_cast<size_t>(N) * 4);
+  p->off_inv = off;
+  off = align_up(off + static_cast<size_t>(N) * 4);
   p->off_done = off;  // per launch and local row tile: R-tile epilogue warps done
   off = align_up(off + static_cast<size_t>(p->n_blocks * p->v_blocks) * (p->Nb / kPairM) * 4);
   p->off_dxf = off;
@@ -348,6 +364,17 @@ size_t flce_workspace_size(int64_t N, int64_t H, int64_t V) {
   Plan p;
   if (!make_plan(N, H, V, &p)) return 0;
   return p.total;
+}
+
+flce_status flce_backward_blocking(int64_t N, int64_t H, int64_t V, int64_t* Nb, int64_t* Vb) {
+  if (!Nb || !Vb || N < 0 || H <= 0 || V <= 0 || H % 8 != 0 || H > kMaxH || N > kMaxDim ||
+      V > kMaxDim)
+    return FLCE_ERR_INVALID_ARG;
+  Plan p;
+  if (!make_plan(N, H, V, &p)) return FLCE_ERR_UNSUPPORTED_SHAPE;
+  *Nb = p.Nb;
+  *Vb = p.Vb;
+  return FLCE_OK;
 }
 
 void flce_set_wait_limit_ns(int64_t limit_ns) {
@@ -447,6 +474,15 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
        reinterpret_cast<uintptr_t>(dW_acc) | reinterpret_cast<uintptr_t>(dX_acc)) & 15)
     return FLCE_ERR_INVALID_ARG;
   if (dX && dX_acc) return FLCE_ERR_INVALID_ARG;
+  // dX is written while X, W, labels and lse are still read (it holds the
+  // gathered rows of X during the call): it may overlap none of them
+  if (dX && N > 0) {
+    const size_t xb = static_cast<size_t>(N) * H * 2;
+    if (overlaps(dX, xb, X, xb) || overlaps(dX, xb, W, static_cast<size_t>(V) * H * 2) ||
+        overlaps(dX, xb, labels, static_cast<size_t>(N) * 8) ||
+        overlaps(dX, xb, lse, static_cast<size_t>(N) * 4))
+      return FLCE_ERR_INVALID_ARG;
+  }
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLCE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -464,15 +500,36 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   const long long* nv = reinterpret_cast<const long long*>(n_valid);
   int* targets = reinterpret_cast<int*>(ws + p.off_t);
   const int S = static_cast<int>(seq_len > 0 ? seq_len : N);
-  // Token tiles whose rows are all ignored have dZ = 0: they add nothing to dW
-  // and their dX rows are 0, so the backward runs on the active tiles only.
+  // Rows without a valid target have dZ = 0: they add nothing to dW and their
+  // dX rows are 0.  Dense rows: when bf16 dX goes through the FP32 accumulator
+  // (V spans several vocab blocks), the rows with a target are gathered to the
+  // front of the dX buffer (free until the final downcast, which puts the rows
+  // back in token order) and the backward runs on ceil(rows / 256) dense
+  // tiles.  Otherwise it runs on the 256-row token tiles that hold a target.
+  const bool dense = dX && !dX_acc && p.v_blocks > 1;
   int* flags = reinterpret_cast<int*>(ws + p.off_flags);
   int* active = reinterpret_cast<int*>(ws + p.off_active);
   int* n_active = active + p.m_tiles;
+  int* toff = reinterpret_cast<int*>(ws + p.off_toff);
+  int* tc = reinterpret_cast<int*>(ws + p.off_tc);
+  float* lc = reinterpret_cast<float*>(ws + p.off_lc);
+  int* inv = reinterpret_cast<int*>(ws + p.off_inv);
   FLCE_CUDA(cudaMemsetAsync(flags, 0, static_cast<size_t>(p.m_tiles) * 4, s));
   FLCE_CUDA(launch_prep_targets(labels, static_cast<int>(N), S, shift, ignore_index, vs,
                                 targets, nullptr, err, s, flags));
-  FLCE_CUDA(launch_compact_tiles(flags, p.m_tiles, active, n_active, s));
+  const void* Xg = X;  // the X rows the backward reads
+  const int* tg = targets;
+  const float* lg = lse;
+  if (dense) {
+    FLCE_CUDA(launch_compact_rows(flags, p.m_tiles, toff, active, n_active, s));
+    FLCE_CUDA(launch_gather_rows(X, targets, lse, toff, static_cast<int>(N), static_cast<int>(H),
+                                 p.m_tiles, dX, tc, lc, inv, s));
+    Xg = dX;
+    tg = tc;
+    lg = lc;
+  } else {
+    FLCE_CUDA(launch_compact_tiles(flags, p.m_tiles, active, n_active, s));
+  }
 
   // the caller's FP32 buffer, or the workspace accumulator when V spans
   // several vocab blocks (a single block writes bf16 dX directly)
@@ -494,10 +551,10 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   if (dX && dx_final) FLCE_CUDA(cudaMemsetAsync(dX, 0, static_cast<size_t>(N) * H * 2, s));
 
   BwdMaps maps;
-  if (!make_tmap(&maps.x_k, X, H, N, H * 2, kBK, kBM) ||
+  if (!make_tmap(&maps.x_k, Xg, H, N, H * 2, kBK, kBM) ||
       !make_tmap(&maps.w_k, W, H, V, H * 2, kBK, kHalfN) ||
       !make_tmap(&maps.w_mn, W, H, V, H * 2, 64, 64) ||
-      !make_tmap(&maps.x_mn, X, H, N, H * 2, 64, 64) ||
+      !make_tmap(&maps.x_mn, Xg, H, N, H * 2, 64, 64) ||
       !make_tmap(&maps.dz_k[0], dz0, p.Vb, p.Nb, p.dz_ld * 2, kBK, kBM) ||
       !make_tmap(&maps.dz_k[1], dz1, p.Vb, p.Nb, p.dz_ld * 2, kBK, kBM) ||
       !make_tmap(&maps.dz_st[0], dz0, p.Vb, p.Nb, p.dz_ld * 2, 64, 32) ||
@@ -507,7 +564,7 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
       !make_tmap_mn3(&maps.dz_mn3[1], dz1, p.Vb, p.Nb, p.dz_ld * 2))
     return FLCE_ERR_CUDA;
   const bool mn3d = H % 64 == 0 && make_tmap_mn3(&maps.w_mn3, W, H, V, H * 2) &&
-                    make_tmap_mn3(&maps.x_mn3, X, H, N, H * 2);
+                    make_tmap_mn3(&maps.x_mn3, Xg, H, N, H * 2);
   if (!mn3d) maps.w_mn3 = maps.x_mn3 = maps.dz_mn3[0];  // unused
   // epilogue targets: FP32 accumulators (reduce-add, 32 x 32 boxes) or the bf16
   // gradients written directly (64 x 32 boxes); an unused map repeats a valid one
@@ -558,8 +615,8 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
   base.N = static_cast<int>(N);
   base.H = static_cast<int>(H);
   base.V = static_cast<int>(V);
-  base.targets = targets;
-  base.lse = lse;
+  base.targets = tg;
+  base.lse = lg;
   base.dz[0] = dz0;
   base.dz[1] = dz1;
   base.dz_ld = static_cast<int>(p.dz_ld);
@@ -632,7 +689,10 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
     }
   }
   prof_end(1, nblk + 1, s);
-  if (dX && !dx_final)
+  if (dense)
+    FLCE_CUDA(launch_downcast_rows(dxf, static_cast<__nv_bfloat16*>(dX), inv, static_cast<int>(N),
+                                   static_cast<int>(H), grad_loss, nv, red, s));
+  else if (dX && !dx_final)
     FLCE_CUDA(launch_downcast(dxf, static_cast<__nv_bfloat16*>(dX), static_cast<size_t>(N) * H,
                               grad_loss, nv, red, s));
   return FLCE_OK;

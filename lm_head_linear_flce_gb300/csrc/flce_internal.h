@@ -151,7 +151,7 @@ struct Plan {
   bool multi_n;           // more than one token block: dW needs an FP32 band
   int launches;           // backward GEMM launches (one per dZ block, plus one)
   size_t off_err, off_t, off_zt, off_part, off_lossp, off_fcnt, off_cnt, off_flags, off_active,
-      off_done, off_dxf, off_dwf, off_dz;
+      off_toff, off_tc, off_lc, off_inv, off_done, off_dxf, off_dwf, off_dz;
   size_t total;
 };
 
@@ -201,7 +201,8 @@ struct VocabSlice {
 
 // Launchers (return cudaGetLastError()).
 // targets[i]: -1 (no valid target), the local column, or kTargetElsewhere.
-// tile_flags (or null): set to 1 for every 256-row tile holding a valid target.
+// tile_flags (or null): for every 256-row tile, its number of rows with a valid
+// target.
 cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int shift,
                                 int64_t ignore_index, const VocabSlice& vs, int* targets,
                                 long long* n_valid, int* err, cudaStream_t st,
@@ -209,6 +210,22 @@ cudaError_t launch_prep_targets(const int64_t* labels, int N, int seq_len, int s
 // active[0 .. *n_active) = indices of the flagged tiles, ascending.
 cudaError_t launch_compact_tiles(const int* tile_flags, int m_tiles, int* active, int* n_active,
                                  cudaStream_t st);
+// Dense rows: toff[0 .. m_tiles] = exclusive scan of the per-tile counts (the
+// last entry: all valid rows), active[t] = t for the ceil(rows / 256) dense
+// tiles, *n_active = their number.
+cudaError_t launch_compact_rows(const int* counts, int m_tiles, int* toff, int* active,
+                                int* n_active, cudaStream_t st);
+// Copies the rows with a valid target of X [N][H] bf16 to the front of xc
+// [N][H] (zeroing the rest of the last dense tile), their targets to tc and
+// lse to lc, and writes inv[i] = the dense index of row i, or -1.  xc must not
+// overlap X.
+cudaError_t launch_gather_rows(const void* X, const int* targets, const float* lse,
+                               const int* toff, int N, int H, int m_tiles, void* xc, int* tc,
+                               float* lc, int* inv, cudaStream_t st);
+// dst row i = bf16_rn(scale * src row inv[i]), or 0 where inv[i] < 0.
+cudaError_t launch_downcast_rows(const float* src, __nv_bfloat16* dst, const int* inv, int N,
+                                 int H, const float* grad_loss, const long long* n_valid,
+                                 int reduction, cudaStream_t st);
 // z_out non-null: a vocabulary shard's (lse, target logit) instead of a loss.
 cudaError_t launch_merge_lse(const float2* partials, int nchunks, int N, const float* zt,
                              const int* targets, float* lse, double* loss_partials,

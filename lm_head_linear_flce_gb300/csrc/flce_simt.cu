@@ -8,7 +8,9 @@ namespace flce {
 
 namespace {
 
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 256;  // one 256-row token tile per block
+static_assert(kPrepThreads == kPairM, "prep blocks are token tiles");
+constexpr int kGatherSlice = 64;   // 16-byte columns of a row per gather block (1 KB)
 constexpr int kMergeThreads = 256;  // rows per block of the shard merge
 constexpr int kMergeGroups = 8;     // warps per block of the log-sum-exp merge
 constexpr int kFinalThreads = 256;
@@ -42,7 +44,6 @@ __global__ void prep_targets_kernel(const int64_t* __restrict__ labels, int N, i
         const int64_t loc = lab - v_offset;
         t = (loc >= 0 && loc < V_local) ? static_cast<int>(loc) : kTargetElsewhere;
         ok = 1;
-        if (tile_flags) tile_flags[i >> 8] = 1;  // this 256-row tile has a target
       } else {
         atomicOr(err, kErrLabel);
       }
@@ -51,6 +52,8 @@ __global__ void prep_targets_kernel(const int64_t* __restrict__ labels, int N, i
   }
   const int cnt = __syncthreads_count(ok);
   if (n_valid && threadIdx.x == 0 && cnt) atomicAdd(n_valid, static_cast<unsigned long long>(cnt));
+  // a block is one 256-row token tile: its count of rows with a valid target
+  if (tile_flags && threadIdx.x == 0) tile_flags[blockIdx.x] = cnt;
 }
 
 // Block sum of the rows' losses in a fixed tree order (FP64), written by
@@ -221,6 +224,128 @@ __global__ void compact_tiles_kernel(const int* __restrict__ flags, int m_tiles,
   if (threadIdx.x == 0) *n_active = base;
 }
 
+// Offsets of each tile's valid rows in the dense row order (an exclusive scan
+// of the per-tile counts; toff[m_tiles] = all valid rows), and the dense
+// row tiles as the backward's tile list: tiles 0 .. ceil(rows / 256) - 1.
+// One block; a block-wide scan per 1024 tiles.
+__global__ void compact_rows_kernel(const int* __restrict__ counts, int m_tiles,
+                                    int* __restrict__ toff, int* __restrict__ active,
+                                    int* __restrict__ n_active) {
+  __shared__ int scan[1024];
+  int base = 0;
+  for (int t0 = 0; t0 < m_tiles; t0 += 1024) {
+    const int t = t0 + threadIdx.x;
+    const int c = t < m_tiles ? counts[t] : 0;
+    scan[threadIdx.x] = c;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+      const int v = threadIdx.x >= off ? scan[threadIdx.x - off] : 0;
+      __syncthreads();
+      scan[threadIdx.x] += v;
+      __syncthreads();
+    }
+    if (t < m_tiles) toff[t] = base + scan[threadIdx.x] - c;
+    base += scan[1023];
+    __syncthreads();
+  }
+  const int tiles = (base + kPairM - 1) / kPairM;
+  for (int t = threadIdx.x; t < tiles; t += blockDim.x) active[t] = t;
+  if (threadIdx.x == 0) {
+    toff[m_tiles] = base;
+    *n_active = tiles;
+  }
+}
+
+// The rows with a valid target, in order, copied to the front of a dense
+// [N][H] bf16 buffer, with their targets and lse beside them; the rows after
+// the last one, to the end of its 256-row tile (and not past N), are zeroed
+// (target -1: dZ = 0, and X = 0 so that the dW contraction stays finite).
+// inv maps every row to its dense index, or -1.  Ignored rows have dZ = 0 and
+// add nothing to dX or dW, so the backward runs on the dense rows only (the
+// cut cross-entropy listing `_patch_model_with_cce` of the Qwen3.5-35B-A3B
+// LoRA SFT blog post relies on the same fact).  Block (b, y): token tile b,
+// 16-byte columns [64 y, 64 y + 64) of each row; block (b, 0) also writes the
+// per-row arrays.
+__global__ void __launch_bounds__(kPairM)
+    gather_rows_kernel(const uint4* __restrict__ X, const int* __restrict__ targets,
+                       const float* __restrict__ lse, const int* __restrict__ toff, int N,
+                       int H8, int m_tiles, uint4* __restrict__ xc, int* __restrict__ tc,
+                       float* __restrict__ lc, int* __restrict__ inv) {
+  __shared__ int rows[kPairM];
+  __shared__ int warp_cnt[kPairM / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x * kPairM + tid;
+  const int t = i < N ? targets[i] : -1;
+  const bool valid = t != -1;
+  const unsigned m = __ballot_sync(0xffffffffu, valid);
+  if (lane == 0) warp_cnt[warp] = __popc(m);
+  __syncthreads();
+  int before = 0, cnt = 0;
+  for (int w = 0; w < kPairM / 32; ++w) {
+    before += w < warp ? warp_cnt[w] : 0;
+    cnt += warp_cnt[w];
+  }
+  const int rank = before + __popc(m & ((1u << lane) - 1u));
+  const int j0 = toff[blockIdx.x];
+  if (valid) rows[rank] = i;
+  if (blockIdx.y == 0) {
+    if (i < N) inv[i] = valid ? j0 + rank : -1;
+    if (valid) {
+      tc[j0 + rank] = t;
+      lc[j0 + rank] = lse[i];
+    }
+  }
+  __syncthreads();
+  const int c0 = blockIdx.y * kGatherSlice;
+  const int c1 = min(H8, c0 + kGatherSlice);
+  for (int r = warp; r < cnt; r += kPairM / 32) {
+    const uint4* src = X + static_cast<size_t>(rows[r]) * H8;
+    uint4* dst = xc + static_cast<size_t>(j0 + r) * H8;
+    for (int c = c0 + lane; c < c1; c += 32) dst[c] = src[c];
+  }
+  const int total = toff[m_tiles];
+  const int pad_end = min(N, (total + kPairM - 1) / kPairM * kPairM);
+  for (int j = total + blockIdx.x; j < pad_end; j += gridDim.x) {
+    for (int c = c0 + tid; c < c1; c += kPairM) xc[static_cast<size_t>(j) * H8 + c] = make_uint4(0, 0, 0, 0);
+    if (blockIdx.y == 0 && tid == 0) {
+      tc[j] = -1;
+      lc[j] = 0.f;
+    }
+  }
+}
+
+// dX row i = bf16_rn(scale * src[inv[i]]) for the rows the backward ran on
+// (scale as in downcast_kernel), 0 for the others: the dense rows' FP32
+// accumulator put back in token order.  A block per row at a time.
+__global__ void downcast_rows_kernel(const float4* __restrict__ src, uint4* __restrict__ dst,
+                                     const int* __restrict__ inv, int N, int H8,
+                                     const float* __restrict__ grad_loss,
+                                     const long long* __restrict__ n_valid, int reduction) {
+  float scale = grad_loss ? *grad_loss : 1.f;
+  if (grad_loss && reduction == 0) {
+    const long long n = *n_valid;
+    scale = n > 0 ? scale / static_cast<float>(n) : 0.f;
+  }
+  for (int row = blockIdx.x; row < N; row += gridDim.x) {
+    const int j = inv[row];
+    uint4* d = dst + static_cast<size_t>(row) * H8;
+    if (j < 0) {
+      for (int c = threadIdx.x; c < H8; c += blockDim.x) d[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const float4* sr = src + static_cast<size_t>(j) * H8 * 2;
+    for (int c = threadIdx.x; c < H8; c += blockDim.x) {
+      const float4 a = sr[2 * c], b = sr[2 * c + 1];
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(scale * a.x, scale * a.y);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(scale * a.z, scale * a.w);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(scale * b.x, scale * b.y);
+      __nv_bfloat162 p3 = __floats2bfloat162_rn(scale * b.z, scale * b.w);
+      d[c] = make_uint4(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1),
+                        *reinterpret_cast<uint32_t*>(&p2), *reinterpret_cast<uint32_t*>(&p3));
+    }
+  }
+}
+
 // Waits on a barrier that nothing will ever complete; the bounded wait must
 // give up, record the timeout and let the kernel return.
 __global__ void selftest_wait_kernel(unsigned long long limit_ns, int* err) {
@@ -302,6 +427,41 @@ cudaError_t launch_downcast(const float* src, __nv_bfloat16* dst, size_t count,
 cudaError_t launch_compact_tiles(const int* tile_flags, int m_tiles, int* active, int* n_active,
                                  cudaStream_t st) {
   compact_tiles_kernel<<<1, 1024, 0, st>>>(tile_flags, m_tiles, active, n_active);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact_rows(const int* counts, int m_tiles, int* toff, int* active,
+                                int* n_active, cudaStream_t st) {
+  compact_rows_kernel<<<1, 1024, 0, st>>>(counts, m_tiles, toff, active, n_active);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* X, const int* targets, const float* lse,
+                               const int* toff, int N, int H, int m_tiles, void* xc, int* tc,
+                               float* lc, int* inv, cudaStream_t st) {
+  if (N <= 0 || m_tiles <= 0) return cudaSuccess;
+  const int H8 = H / 8;
+  const dim3 grid(m_tiles, (H8 + kGatherSlice - 1) / kGatherSlice);
+  gather_rows_kernel<<<grid, kPairM, 0, st>>>(static_cast<const uint4*>(X), targets, lse, toff,
+                                              N, H8, m_tiles, static_cast<uint4*>(xc), tc, lc,
+                                              inv);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_downcast_rows(const float* src, __nv_bfloat16* dst, const int* inv, int N,
+                                 int H, const float* grad_loss, const long long* n_valid,
+                                 int reduction, cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int blocks = N < sms * 16 ? N : sms * 16;
+  downcast_rows_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(src),
+                                               reinterpret_cast<uint4*>(dst), inv, N, H / 8,
+                                               grad_loss, n_valid, reduction);
   note_launch();
   return cudaGetLastError();
 }

@@ -238,3 +238,25 @@ def test_w_block_kept_within_64_mib(lib):
     # (the per-launch counters grow a little with twice as many blocks)
     assert abs((wide - auto) - 2 * N * 4096 * 2) <= 64 * 1024, wide - auto
     assert lib.flce_workspace_size(8192, 3584, 152064) == qwen2_by_hand
+
+
+def test_backward_blocking_of_the_five_workloads(lib):
+    """flce_backward_blocking reports the automatic dZ block (include/flce.h,
+    flce_set_backward_block): every row in one token block for all five
+    workloads; 4096 vocab columns where V spans several blocks (the 32 Mi /
+    64 Mi element caps, the 76-dW-tile growth at 32K rows, the 64 MiB W-row
+    cap at H = 8192); the whole 4096-column vocabulary of the tiny workload in
+    one block, which keeps it on token tiles rather than dense rows."""
+    import ctypes
+    fn = lib.flce_backward_blocking
+    fn.argtypes = [ctypes.c_int64] * 3 + [ctypes.POINTER(ctypes.c_int64)] * 2
+    fn.restype = ctypes.c_int
+    want = {(256, 256, 4096): (256, 4096), (8192, 3584, 152064): (8192, 4096),
+            (16384, 4096, 151936): (16384, 4096), (32768, 2048, 151936): (32768, 4096),
+            (4096, 8192, 128256): (4096, 4096)}
+    for (N, H, V), blk in want.items():
+        nb, vb = ctypes.c_int64(), ctypes.c_int64()
+        assert fn(N, H, V, ctypes.byref(nb), ctypes.byref(vb)) == 0
+        assert (nb.value, vb.value) == blk, (N, H, V, nb.value, vb.value)
+    nb, vb = ctypes.c_int64(), ctypes.c_int64()
+    assert fn(8192, 3583, 152064, ctypes.byref(nb), ctypes.byref(vb)) != 0  # H % 8 != 0

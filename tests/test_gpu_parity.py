@@ -299,3 +299,34 @@ def test_forward_row_bands_with_a_ragged_last_band():
     N, H, V = 2800, 8192, 3000
     X, W, labels = workloads.random_case(N, H, V, seed=41, x_std=0.5, w_std=0.01)
     check_against_oracle(X, W, labels, reduction="sum", grad=0.5)
+
+
+@pytest.mark.parametrize("ignore_frac", [0.45, 0.0, 0.97])
+def test_dense_rows_are_gathered_and_put_back(ignore_frac):
+    # rows without a target scattered through every 256-row tile, several vocab
+    # blocks (256 columns each), ragged N and a per-sequence shift: the
+    # backward gathers the rows with a target into dense tiles inside dX's
+    # buffer and runs on those; dX comes back in token order with the other
+    # rows exactly 0.  Also: no row ignored (all gathered), nearly all ignored
+    # (one dense tile, mostly padding).
+    flce.flce_set_backward_block(1024, 1024 * 256)
+    N, H, V, S = 1000, 136, 1300, 500
+    X, W, labels = workloads.random_case(N, H, V, seed=91, ignore_frac=ignore_frac, w_std=0.1)
+    assert flce.flce_backward_blocking(N, H, V) == (1024, 256)
+    got, ref = check_against_oracle(X, W, labels, seq_len=S, shift=True, grad=0.5)
+    t = torch.full((N,), -100, dtype=torch.int64)
+    t.view(-1, S)[:, :-1] = labels.view(-1, S)[:, 1:]
+    ignored = (t == -100).numpy()
+    assert not got["dX"][ignored].any()
+    assert got["dX"][~ignored].any(axis=1).all()
+
+
+def test_dx_overlapping_an_input_is_refused():
+    dev = torch.device("cuda")
+    X, W, labels = workloads.random_case(300, 64, 700, seed=92)
+    Xd, Wd, Ld = X.to(dev), W.to(dev), labels.to(dev)
+    _, lse, nv, ws = flce.flce_forward(Xd, Wd, Ld)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+    for alias in (Xd, Wd[:300]):
+        with pytest.raises(flce.FlceError):
+            flce.flce_backward(Xd, Wd, Ld, lse, nv, g, dX=alias, need_dW=False, workspace=ws)
