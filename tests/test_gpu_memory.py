@@ -31,9 +31,10 @@ def documented_bound(N, H, V):
     """Upper bound of flce_workspace_size from the layout in include/flce.h:
     FP32 dX [N][H]; an FP32 dW band of at most 2^27 / 256 vocab rows; two dZ
     blocks of at most 2^27 bf16 elements plus 64 padding columns per row; 128
-    (max, sum-exp) pairs per row; 1 MiB of counters, flags and targets."""
+    (max, sum-exp) pairs per row; 16 bytes per row of targets and dense-row
+    maps; 1 MiB of counters and flags."""
     return (4 * N * H + 4 * H * min(V, (1 << 27) // 256) + 2 * 2 * ((1 << 27) + 64 * N)
-            + 8 * 128 * N + MiB)
+            + 8 * 128 * N + 16 * N + MiB)
 
 
 def device_inputs(wl):
