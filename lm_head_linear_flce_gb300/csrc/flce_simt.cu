@@ -297,16 +297,28 @@ __global__ void __launch_bounds__(kPairM)
   }
   __syncthreads();
   const int c0 = blockIdx.y * kGatherSlice;
-  const int c1 = min(H8, c0 + kGatherSlice);
-  for (int r = warp; r < cnt; r += kPairM / 32) {
-    const uint4* src = X + static_cast<size_t>(rows[r]) * H8;
-    uint4* dst = xc + static_cast<size_t>(j0 + r) * H8;
-    for (int c = c0 + lane; c < c1; c += 32) dst[c] = src[c];
+  const int width = min(H8, c0 + kGatherSlice) - c0;
+  // (row, column) pairs of the slice, four loads in flight per thread
+  const int total = cnt * width;
+  for (int e0 = tid; e0 < total; e0 += 4 * kPairM) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * kPairM;
+      if (e < total)
+        v[u] = X[static_cast<size_t>(rows[e / width]) * H8 + c0 + e % width];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * kPairM;
+      if (e < total) xc[static_cast<size_t>(j0 + e / width) * H8 + c0 + e % width] = v[u];
+    }
   }
-  const int total = toff[m_tiles];
-  const int pad_end = min(N, (total + kPairM - 1) / kPairM * kPairM);
-  for (int j = total + blockIdx.x; j < pad_end; j += gridDim.x) {
-    for (int c = c0 + tid; c < c1; c += kPairM) xc[static_cast<size_t>(j) * H8 + c] = make_uint4(0, 0, 0, 0);
+  const int rows_total = toff[m_tiles];
+  const int pad_end = min(N, (rows_total + kPairM - 1) / kPairM * kPairM);
+  for (int j = rows_total + blockIdx.x; j < pad_end; j += gridDim.x) {
+    for (int c = c0 + tid; c < c0 + width; c += kPairM)
+      xc[static_cast<size_t>(j) * H8 + c] = make_uint4(0, 0, 0, 0);
     if (blockIdx.y == 0 && tid == 0) {
       tc[j] = -1;
       lc[j] = 0.f;
