@@ -260,10 +260,11 @@ __global__ void compact_rows_kernel(const int* __restrict__ counts, int m_tiles,
 // [N][H] bf16 buffer, with their targets and lse beside them; the rows after
 // the last one, to the end of its 256-row tile (and not past N), are zeroed
 // (target -1: dZ = 0, and X = 0 so that the dW contraction stays finite).
-// inv maps every row to its dense index, or -1.  Ignored rows have dZ = 0 and
-// add nothing to dX or dW, so the backward runs on the dense rows only (the
-// cut cross-entropy listing `_patch_model_with_cce` of the Qwen3.5-35B-A3B
-// LoRA SFT blog post relies on the same fact).  Block (b, y): token tile b,
+// inv maps every row to its dense index, or -1.  A row without a valid target
+// has no term in the loss (the ignore_index call of the Qwen3.5-35B-A3B LoRA
+// SFT blog post, listing `_patch_model_with_cce`), so its dZ row is 0 and it
+// adds nothing to dX or dW: the backward runs on the dense rows only.
+// Block (b, y): token tile b,
 // 16-byte columns [64 y, 64 y + 64) of each row; block (b, 0) also writes the
 // per-row arrays.
 __global__ void __launch_bounds__(kPairM)
