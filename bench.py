@@ -481,14 +481,15 @@ def run_row(args, world, rank, local):
     else:
         ws = torch.empty(flce.workspace_size(N, H, V), dtype=torch.uint8, device=dev)
         dX = torch.empty_like(X)
+        rows = backward_rows(wl, L.cpu())  # the backward runs on these rows only
         if args.row == "dx_only":
-            flops = 6 * N * H * V
+            flops = 2 * N * H * V + 4 * rows * H * V
 
             def step():
                 _, lse, nv, _ = flce.flce_forward(X, W, L, workspace=ws, **kw)
                 flce.flce_backward(X, W, L, lse, nv, g, workspace=ws, dX=dX, need_dW=False, **kw)
         elif args.row == "accumulate":
-            flops = 8 * N * H * V
+            flops = 2 * N * H * V + 6 * rows * H * V
             dW_acc = torch.zeros(V, H, dtype=torch.float32, device=dev)
 
             def step():
