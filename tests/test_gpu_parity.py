@@ -330,3 +330,14 @@ def test_dx_overlapping_an_input_is_refused():
     for alias in (Xd, Wd[:300]):
         with pytest.raises(flce.FlceError):
             flce.flce_backward(Xd, Wd, Ld, lse, nv, g, dX=alias, need_dW=False, workspace=ws)
+
+
+def test_dense_rows_beyond_one_scan_chunk():
+    # 1172 token tiles and about 1055 dense tiles: the one-block scan of the
+    # per-tile counts and the dense tile list both span two 1024-tile chunks;
+    # 37 token blocks (dW through the FP32 band) x 5 vocab blocks
+    flce.flce_set_backward_block(8192, 8192 * 256)
+    N, H, V = 300000, 32, 1200
+    assert flce.flce_backward_blocking(N, H, V) == (8192, 256)
+    X, W, labels = workloads.random_case(N, H, V, seed=93, w_std=0.5)
+    check_against_oracle(X, W, labels, reduction="sum", grad=0.5)
