@@ -105,12 +105,14 @@ flce_status flce_forward(const void* X, const void* W, const int64_t* labels,
  *   lse, n_valid    device, as written by flce_forward for the same inputs.
  *   grad_loss       device float, 1 element: g = d(outer loss)/d(loss).
  *   dX              device bf16 [N, H] or NULL to skip it (e.g. when only W is
- *                   trained); written, not accumulated.  It must not overlap
- *                   X, W, labels or lse (FLCE_ERR_INVALID_ARG): while the call
- *                   runs it may hold a dense copy of the rows of X that have a
+ *                   trained); written, not accumulated.  While the call runs
+ *                   it may hold a dense copy of the rows of X that have a
  *                   valid target.
  *   dW              device bf16 [V, H] or NULL to skip it (a frozen LM head,
  *                   as in LoRA fine-tuning); written, not accumulated.
+ * No output may overlap an input (X, W, labels, lse, n_valid, grad_loss), the
+ * workspace or the other output: FLCE_ERR_INVALID_ARG (so for every backward
+ * entry point, with dW_acc and dX_acc as outputs).
  * Gradients are accumulated in FP32 and rounded to bf16 (round to nearest even)
  * once, after the scale g / n_valid (mean) or g (sum) is applied in FP32.
  * Rows without a valid target contribute nothing: with dX requested and V

@@ -474,14 +474,27 @@ flce_status backward_impl(const void* X, const void* W, const int64_t* labels, i
        reinterpret_cast<uintptr_t>(dW_acc) | reinterpret_cast<uintptr_t>(dX_acc)) & 15)
     return FLCE_ERR_INVALID_ARG;
   if (dX && dX_acc) return FLCE_ERR_INVALID_ARG;
-  // dX is written while X, W, labels and lse are still read (it holds the
-  // gathered rows of X during the call): it may overlap none of them
-  if (dX && N > 0) {
-    const size_t xb = static_cast<size_t>(N) * H * 2;
-    if (overlaps(dX, xb, X, xb) || overlaps(dX, xb, W, static_cast<size_t>(V) * H * 2) ||
-        overlaps(dX, xb, labels, static_cast<size_t>(N) * 8) ||
-        overlaps(dX, xb, lse, static_cast<size_t>(N) * 4))
-      return FLCE_ERR_INVALID_ARG;
+  // The outputs are written while the inputs and the workspace are still read
+  // (dX even holds the gathered rows of X during the call): no output may
+  // overlap an input, the workspace or another output.
+  {
+    struct Range {
+      const void* p;
+      size_t n;
+    };
+    const size_t nh = static_cast<size_t>(N) * H, vh = static_cast<size_t>(V) * H;
+    const Range outs[] = {{dX, nh * 2}, {dW, vh * 2}, {dW_acc, vh * 4}, {dX_acc, nh * 4}};
+    const Range ins[] = {{X, nh * 2},       {W, vh * 2},        {labels, static_cast<size_t>(N) * 8},
+                         {lse, static_cast<size_t>(N) * 4}, {n_valid, 8}, {grad_loss, 4},
+                         {workspace, workspace_bytes}};
+    for (int a = 0; a < 4; ++a) {
+      if (!outs[a].p) continue;
+      for (const Range& r : ins)
+        if (r.p && overlaps(outs[a].p, outs[a].n, r.p, r.n)) return FLCE_ERR_INVALID_ARG;
+      for (int b = a + 1; b < 4; ++b)
+        if (outs[b].p && overlaps(outs[a].p, outs[a].n, outs[b].p, outs[b].n))
+          return FLCE_ERR_INVALID_ARG;
+    }
   }
   DeviceInfo dev;
   if ((st = device_info(&dev)) != FLCE_OK) return st;

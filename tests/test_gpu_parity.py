@@ -321,15 +321,25 @@ def test_dense_rows_are_gathered_and_put_back(ignore_frac):
     assert got["dX"][~ignored].any(axis=1).all()
 
 
-def test_dx_overlapping_an_input_is_refused():
+def test_outputs_overlapping_inputs_or_each_other_are_refused():
+    # refused on the host before anything is enqueued (include/flce.h,
+    # flce_backward): dX on X or on W's rows, dW on W, dX inside dW, an
+    # output inside the workspace; separate buffers still work afterwards
     dev = torch.device("cuda")
     X, W, labels = workloads.random_case(300, 64, 700, seed=92)
     Xd, Wd, Ld = X.to(dev), W.to(dev), labels.to(dev)
     _, lse, nv, ws = flce.flce_forward(Xd, Wd, Ld)
     g = torch.ones(1, dtype=torch.float32, device=dev)
-    for alias in (Xd, Wd[:300]):
-        with pytest.raises(flce.FlceError):
-            flce.flce_backward(Xd, Wd, Ld, lse, nv, g, dX=alias, need_dW=False, workspace=ws)
+    dW_big = torch.empty_like(Wd)
+    ws_view = ws[: 300 * 64 * 2].view(torch.bfloat16).view(300, 64)
+    cases = [dict(dX=Xd, need_dW=False), dict(dX=Wd[:300], need_dW=False),
+             dict(dW=Wd, need_dX=False), dict(dX=dW_big[:300], dW=dW_big),
+             dict(dX=ws_view, need_dW=False)]
+    for kw in cases:
+        with pytest.raises(flce.FlceError, match="INVALID_ARG"):
+            flce.flce_backward(Xd, Wd, Ld, lse, nv, g, workspace=ws, **kw)
+    dX, dW, _ = flce.flce_backward(Xd, Wd, Ld, lse, nv, g, workspace=ws)
+    assert torch.isfinite(dX.float()).all() and torch.isfinite(dW.float()).all()
 
 
 def test_dense_rows_beyond_one_scan_chunk():
