@@ -69,11 +69,11 @@ struct GemmArgs {
   unsigned long long wait_limit_ns;
 };
 
-// One dZ block of the backward: the active 256-row token tiles
-// active[tile0 .. tile0 + mt) (at most `mt`; fewer when tiles whose rows are all
-// ignored were dropped) x vocab columns [col0, col0 + vt*256), stored in dZ
-// slot `slot`.  Local dZ row l of the block is token row
-// active[tile0 + l / 256] * 256 + l % 256.
+// One dZ block of the backward: the 256-row tiles active[tile0 .. tile0 + mt)
+// (at most `mt`; fewer when rows without a target were left out) x vocab
+// columns [col0, col0 + vt*256), stored in dZ slot `slot`.  Local dZ row l of
+// the block is row active[tile0 + l / 256] * 256 + l % 256 of the X the
+// backward reads (a token row, or a dense row of the gathered copy).
 struct BlockDesc {
   int tile0, col0;
   int mt;     // at most this many 256-row token tiles
@@ -115,13 +115,15 @@ struct BwdArgs {
                    // after its R tiles
   int want_dx, want_dw;  // which contractions run (dX tiles, dW tiles)
   int h_tiles;           // 256-column tiles of H
-  const int* active;     // active 256-row token tiles, ascending
+  const int* active;     // 256-row tiles of the rows the backward reads, ascending:
+                         // the token tiles holding a target, or 0, 1, ... over
+                         // the dense rows gathered to the front of X's copy
   const int* n_active;   // number of entries of `active`
   int kb_h;  // K blocks of the recompute (ceil(H / 64))
   int mn3d;  // 1: MN-major halves load as one 3-D box (w_mn3 / x_mn3 / dz_mn3)
   int N, H, V;
-  const int* targets;
-  const float* lse;
+  const int* targets;  // per row of that X (token rows, or the dense rows)
+  const float* lse;     // likewise
   __nv_bfloat16* dz[2];
   int dz_ld;
   float* dxf;                  // FP32 dX accumulator [N][H], or null
