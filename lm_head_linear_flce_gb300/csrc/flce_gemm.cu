@@ -613,10 +613,10 @@ struct Tile {
   int kind, m0, n0, k_blocks;
 };
 
-// Tiles of this launch, from the number of active token tiles (written on the
-// device before the first backward launch).
+// Tiles of this launch, from the number of 256-row tiles the backward runs on
+// (written on the device before the first backward launch).
 struct Counts {
-  int mt_r, mt_w;  // active token tiles of the R block and of the W block
+  int mt_r, mt_w;  // 256-row tiles of the R block and of the W block
   int r_tiles, x_tiles, w_tiles, total;
   int lag;         // X tiles of row tile m follow the R tiles of row tile m + lag
   int first;       // R tiles handed out before the W tiles when w_early
@@ -641,7 +641,8 @@ __device__ __forceinline__ Counts tile_counts(const BwdArgs& a) {
   return c;
 }
 
-// First token row of local dZ row `l` of a block starting at active tile tile0.
+// Row of the X the backward reads (a token row, or a dense row of the gathered
+// copy) of local dZ row `l` of a block starting at tile-list entry tile0.
 __device__ __forceinline__ int token_row(const BwdArgs& a, int tile0, int l) {
   return a.active[tile0 + (l >> 8)] * kPairM + (l & (kPairM - 1));
 }
