@@ -260,3 +260,30 @@ def test_backward_blocking_of_the_five_workloads(lib):
         assert (nb.value, vb.value) == blk, (N, H, V, nb.value, vb.value)
     nb, vb = ctypes.c_int64(), ctypes.c_int64()
     assert fn(8192, 3583, 152064, ctypes.byref(nb), ctypes.byref(vb)) != 0  # H % 8 != 0
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="made-up device addresses: only where no kernel can run")
+def test_backward_refuses_outputs_that_overlap_on_the_host(lib):
+    """No output may overlap an input, the workspace or another output
+    (include/flce.h, flce_backward): refused with FLCE_ERR_INVALID_ARG on the
+    host, before anything is enqueued.  Made-up, suitably aligned addresses
+    stand in for device buffers."""
+    N, H, V = 512, 64, 1000
+    nh = N * H * 2
+    base = 1 << 40
+    X, W = base, base + (1 << 30)
+    labels, lse, nv, g = base + (2 << 30), base + (3 << 30), base + (4 << 30), base + (5 << 30)
+    ws, wsn = base + (6 << 30), lib.flce_workspace_size(N, H, V)
+    dX, dW = base + (8 << 30), base + (9 << 30)
+    fn = lib.flce_backward
+    P = ctypes.c_void_p
+
+    def call(dx, dw):
+        return fn(P(X), P(W), P(labels), N, H, V, 0, -100, 0, 0, P(lse), P(nv), P(g),
+                  P(dx), P(dw), P(ws), wsn, None)
+
+    for dx, dw in [(X, None), (X + nh - 16, None), (W, None), (None, W + 256),
+                   (dX, dX + nh - 16), (dW + 4096, dW), (ws + 256, None), (None, ws),
+                   (lse - 16 * 64, None), (None, labels)]:
+        assert call(dx, dw) == 1, (dx, dw)
