@@ -218,6 +218,31 @@ def test_ignored_rows_are_inert():
     assert a["loss"] == b["loss"]
 
 
+@pytest.mark.parametrize("reduction", ["mean", "sum"])
+def test_rows_without_a_target_drop_out(reduction):
+    """Loss, lse and dW over all rows equal those over the rows that have a
+    target alone (gathered in order, the shift applied first), and their dX
+    rows are the same; the other rows' dX is exactly 0.  The mean's
+    denominator counts the same rows either way.  (What lets a backward run on
+    the rows with a target only.)"""
+    B, S, H, V = 2, 40, 11, 37
+    X, W, labels = _rand(B * S, H, V, 21, ignore_frac=0.45)
+    t, valid, n_valid, _ = oracle.effective_targets(labels, V, seq_len=S, shift=True)
+    rows = np.nonzero(valid)[0]
+    assert 0 < len(rows) < B * S
+    full = oracle.forward(X, W, labels, seq_len=S, shift=True, reduction=reduction)
+    dX, dW = oracle.backward(X, W, labels, seq_len=S, shift=True, reduction=reduction,
+                             grad_loss=0.7)
+    dense = oracle.forward(X[rows], W, t[rows], reduction=reduction)
+    dXd, dWd = oracle.backward(X[rows], W, t[rows], reduction=reduction, grad_loss=0.7)
+    assert dense["n_valid"] == full["n_valid"] == n_valid == len(rows)
+    assert dense["loss"] == pytest.approx(full["loss"], rel=1e-13)
+    np.testing.assert_allclose(dense["lse"], full["lse"][rows], rtol=1e-14)
+    np.testing.assert_allclose(dWd, dW, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dXd, dX[rows], rtol=1e-12, atol=1e-15)
+    assert np.all(dX[~valid] == 0.0)
+
+
 def test_shift_has_no_leak_across_sequences():
     B, S, H, V = 3, 7, 5, 19
     X, W, labels = _rand(B * S, H, V, 8, ignore_frac=0.1)
