@@ -23,7 +23,7 @@
  *   - Everything is enqueued on `stream` and runs asynchronously; no entry point
  *     synchronises except flce_get_error.
  *   - X and W are bf16, row-major, rows contiguous: X[i*H + h], W[v*H + h].
- *     H must be a multiple of 8 (16-byte rows for the tensor-memory copies) and
+ *     H must be a multiple of 8 (16-byte rows for the TMA tensor copies) and
  *     both base pointers 16-byte aligned.
  *   - labels are int64.  With shift != 0, row s of each length-seq_len sequence
  *     is scored against labels[s+1] of the same sequence and the last row of
@@ -36,9 +36,10 @@
  *     completes.
  *   - reduction MEAN divides by n_valid, the number of valid targets in the
  *     whole call; with n_valid == 0 the loss and gradients are 0.
- *   - Host-detectable errors (null pointers, bad sizes, short workspace, a
- *     device older than sm_103) are returned at once and nothing is enqueued.
- *     No exception crosses the ABI and no kernel traps.
+ *   - Host-detectable errors (null pointers, bad sizes, short workspace,
+ *     overlapping outputs of a backward call, a device older than sm_103) are
+ *     returned at once and nothing is enqueued.  No exception crosses the ABI
+ *     and no kernel traps.
  */
 #ifndef FLCE_H
 #define FLCE_H
